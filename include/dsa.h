@@ -1,0 +1,165 @@
+/*
+ * dsa.h - C ABI of the GB300 (sm_103a) DSA sparse MLA attention library (libdsa_gb300.so).
+ *
+ * What the library computes is defined by sglang PR #38547 "Enable zero-RoPE TileLang DSA on
+ * gfx950":
+ *   - Summary / Contract table: the 256+0 latent geometry (256-wide NoPE latent, zero-width
+ *     RoPE tail; Q [tokens, 64, 256], KV [slots, 1, 256], output BF16 [tokens, 64, 256]) and
+ *     the DeepSeek-style 512+64 layout kept as a control (d_v = 512, 64-wide RoPE tail);
+ *   - Contract table, "scaled FP8 cache row": 264 bytes = 256 e4m3 + 2 fp32 scales + 0 RoPE,
+ *     656 bytes = 512 e4m3 + 4 fp32 scales + 64 bf16 RoPE values;
+ *   - Scope list: quant_k_cache (pack rows), dequant_k_cache (direct, paged, gather/dequant);
+ *   - Direct GLM geometry coverage list: top-k widths 2048 / 2112, rows padded with -1,
+ *     "gather/mask/score/softmax/value", bit-identical repeated execution.
+ *
+ * Conventions for every entry point:
+ *   - All pointers are DEVICE pointers unless stated otherwise; the caller owns all memory.
+ *     The library allocates nothing and keeps no per-call state, so calls on different
+ *     streams may run concurrently when they use different output/workspace buffers.
+ *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL = legacy default
+ *     stream) and runs asynchronously. The return value reports host-side argument checks and
+ *     launch errors only. Problems found on the device (an index that addresses no slot, a
+ *     bounded wait that timed out) are OR-ed into the optional device word `error_word`
+ *     (DSA_DEVERR_* bits), which the caller reads after synchronising.
+ *   - bf16 tensors are IEEE bfloat16 bit patterns (uint16); all strides are in elements.
+ *   - On error nothing is launched and no output is written.
+ */
+#ifndef DSA_GB300_H
+#define DSA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DSA_API __attribute__((visibility("default")))
+#else
+#define DSA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARGUMENT = 1,   /* null pointer, negative size, bad stride or alignment */
+  DSA_ERR_UNSUPPORTED = 2,        /* a geometry or head count this build has no kernel for */
+  DSA_ERR_WORKSPACE_TOO_SMALL = 3,
+  DSA_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed (see dsa_last_cuda_error) */
+  DSA_ERR_NO_DEVICE = 5           /* the current device is not an sm_103 GPU */
+} dsa_status_t;
+
+/* Bits OR-ed into the optional device error word. */
+#define DSA_DEVERR_INDEX_OUT_OF_RANGE 0x1  /* an index / page addressed no slot: entry masked */
+#define DSA_DEVERR_TIMEOUT 0x2             /* a bounded device-side wait gave up */
+#define DSA_DEVERR_SLOT_OUT_OF_RANGE 0x4   /* quant_k_cache: out_loc outside [0, num_slots): row skipped */
+
+typedef enum {
+  DSA_CACHE_BF16 = 0,        /* bf16 latent rows [num_slots, d_nope + d_rope] */
+  DSA_CACHE_FP8_SCALED = 1   /* packed rows [num_slots, dsa_packed_row_bytes(d_nope, d_rope)] uint8 */
+} dsa_cache_kind_t;
+
+/* Human-readable name of a status code (static string). */
+DSA_API const char* dsa_status_string(dsa_status_t status);
+
+/* The CUDA error code (cudaError_t as int) behind the last DSA_ERR_CUDA of this thread. */
+DSA_API int dsa_last_cuda_error(void);
+
+/* Bytes of one packed scaled-FP8 row: d_nope codes + 4 * (d_nope / 128) scale bytes +
+ * 2 * d_rope RoPE bytes (Contract table: 264 for 256+0, 656 for 512+64). Returns -1 when
+ * d_nope is not a positive multiple of 128 or d_rope < 0. */
+DSA_API int64_t dsa_packed_row_bytes(int d_nope, int d_rope);
+
+/* Bytes of one cache row of the given kind (bf16 rows: 2 * (d_nope + d_rope)). */
+DSA_API int64_t dsa_cache_row_bytes(dsa_cache_kind_t kind, int d_nope, int d_rope);
+
+/*
+ * dsa_quant_k_cache - pack latent rows into the scaled-FP8 cache (quant_k_cache, Scope list;
+ * memory_pool write sites). For row i and each 128-element tile j of its NoPE part:
+ *   amax = max |x|, scale = amax / 448 (fp32), code = e4m3_rne_satfinite(x / scale) (one IEEE
+ *   fp32 division per element; an all-zero tile stores scale 0 and codes 0),
+ * written to slot out_loc[i] (or slot i when out_loc is NULL) as
+ *   [d_nope codes][d_nope/128 fp32 scales, little endian][d_rope bf16 RoPE values, copied].
+ *   k_nope        bf16 [n, d_nope], row i at k_nope + i * k_nope_row_stride (stride >= d_nope, even)
+ *   k_rope        bf16 [n, d_rope], row i at k_rope + i * k_rope_row_stride; NULL iff d_rope == 0
+ *   out_loc       int64 [n] destination slots, or NULL; a slot outside [0, num_slots) skips the row
+ *                 and sets DSA_DEVERR_SLOT_OUT_OF_RANGE
+ *   cache         uint8 [num_slots, row_bytes], 8-byte aligned base
+ * Supported: d_nope in {256, 512}, d_rope in {0, 64}. n == 0 is a no-op.
+ */
+DSA_API dsa_status_t dsa_quant_k_cache(const void* k_nope, int64_t k_nope_row_stride, const void* k_rope,
+                               int64_t k_rope_row_stride, int64_t n, int d_nope, int d_rope,
+                               const int64_t* out_loc, void* cache, int64_t num_slots,
+                               int32_t* error_word, void* stream);
+
+/*
+ * dsa_gather_dequant - gather latent rows by index and widen them to bf16 (dequant_k_cache:
+ * direct, paged and gather/dequant paths; Contract table "paged dequant/gather").
+ *   indices       int32 [n]; an entry < 0 yields a zero row
+ *   block_table   int32 [R, bt_stride] physical page of each logical page, or NULL (direct mode:
+ *                 the index is the slot). Paged: slot = block_table[r, i / page_size] * page_size
+ *                 + i % page_size with r = req_of_index[k] (0 when req_of_index is NULL) and
+ *                 i < max_pages * page_size.
+ *   out           bf16 [n, d_nope + d_rope] (contiguous). FP8 rows: bf16_rne(fp32(e4m3(code)) * scale),
+ *                 RoPE bits copied; BF16 rows: copied.
+ * An index that addresses no slot yields a zero row and sets DSA_DEVERR_INDEX_OUT_OF_RANGE.
+ */
+DSA_API dsa_status_t dsa_gather_dequant(const void* cache, dsa_cache_kind_t kind, int64_t num_slots,
+                                int d_nope, int d_rope, const int32_t* indices, int64_t n,
+                                const int32_t* block_table, int64_t bt_stride, int page_size,
+                                int max_pages, const int32_t* req_of_index, void* out,
+                                int32_t* error_word, void* stream);
+
+/* Arguments of dsa_sparse_attn. Zero-initialise, then fill. */
+typedef struct dsa_attn_args {
+  const void* q;                 /* bf16 [T, H, d_nope + d_rope]; element (t,h,d) at
+                                    q + t*q_stride_t + h*q_stride_h + d; 16-byte aligned base,
+                                    strides multiples of 8 elements */
+  int64_t q_stride_t, q_stride_h;
+  int64_t T;                     /* query tokens (0 = no-op) */
+  int H;                         /* heads: 64 */
+  const void* cache;             /* BF16 rows or packed FP8 rows, see dsa_cache_kind_t */
+  dsa_cache_kind_t kind;
+  int64_t num_slots;
+  int d_nope, d_rope, d_v;       /* (256, 0, 256) or (512, 64, 512) */
+  const int32_t* indices;        /* int32 [T, topk] at indices + t*idx_stride_t; < 0 = masked */
+  int64_t idx_stride_t;
+  int topk;                      /* 1 .. 16384 */
+  const int32_t* block_table;    /* int32 [R, bt_stride] or NULL (direct slots) */
+  int64_t bt_stride;
+  int page_size, max_pages;
+  const int32_t* req_of_token;   /* int32 [T] request of each token, or NULL (request 0) */
+  float sm_scale;                /* softmax scale applied to q.k */
+  void* out;                     /* bf16 [T, H, d_v]; (t,h,d) at out + t*out_stride_t + h*out_stride_h + d */
+  int64_t out_stride_t, out_stride_h;
+  float* lse;                    /* optional fp32 [T, H] natural-log sum of exp(scores); NULL ok */
+  void* workspace;               /* device scratch of dsa_sparse_attn_workspace_size bytes,
+                                    zero-filled before its first use; every call leaves it
+                                    zero-filled again. One call at a time per workspace. */
+  size_t workspace_bytes;
+  int32_t* error_word;           /* optional device int32; DSA_DEVERR_* bits are OR-ed in */
+} dsa_attn_args_t;
+
+/*
+ * dsa_sparse_attn_workspace_size - bytes of workspace dsa_sparse_attn needs for these arguments
+ * on the current device (depends on the device's SM count and d_v only).
+ */
+DSA_API dsa_status_t dsa_sparse_attn_workspace_size(const dsa_attn_args_t* args, size_t* bytes);
+
+/*
+ * dsa_sparse_attn - DSA sparse MLA attention forward (the TileLang BF16 "partial" kernel and
+ * the FP8 kernel of the Scope list, re-designed for sm_103a). For every token t and head h:
+ *   valid entries j: indices[t, j] >= 0 (translated through block_table in paged mode);
+ *   k_j = the latent row (BF16 as stored; FP8: e4m3 code * tile scale, RoPE bf16 as stored);
+ *   s_j = sm_scale * dot(q[t,h,:], k_j), p = softmax_j(s), out[t,h,:] = sum_j p_j * k_j[0:d_v];
+ *   lse[t,h] = log(sum_j exp(s_j)). A token with no valid entry gets out = 0 and lse = -inf.
+ * Duplicate indices are separate terms. The result is bit-identical across repeated calls with
+ * the same inputs on the same device.
+ */
+DSA_API dsa_status_t dsa_sparse_attn(const dsa_attn_args_t* args, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_GB300_H */

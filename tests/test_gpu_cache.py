@@ -1,0 +1,135 @@
+"""GPU parity of the packed-cache kernels against the oracle: dsa_quant_k_cache must be
+bit-exact (e4m3 RNE codes, fp32 amax/448 scales, RoPE bytes), and dsa_gather_dequant must
+be bit-exact (bf16_rne(fp32(code) * scale)), in direct and paged modes, for the 264-byte
+(256+0) and 656-byte (512+64) rows (sglang PR #38547, Contract table and Scope list)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import dsa_sparse_attention_mla_gb300 as dsa
+from dsa_sparse_attention_mla_gb300 import workloads as W
+
+from _helpers import bf16_dev, bits_of
+
+pytestmark = pytest.mark.gpu
+
+
+def _special_rows(n, D, seed):
+    rows = W.NormalRows(seed, 1, n, D).bits().copy()
+    rows[0] = 0                                       # all-zero tiles -> scale 0
+    rows[1, :] = 0x8000                               # all -0.0
+    rows[2, 5] = 0x7F7F                               # a huge value in one tile
+    rows[3, :128] = 0x3F80                            # constant tile
+    x = torch.from_numpy(rows[4].view(np.int16)).view(torch.bfloat16).float() * 1e-30
+    rows[4] = x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)   # tiny values (subnormal codes)
+    return rows
+
+
+@pytest.mark.parametrize("d_nope,d_rope", [(256, 0), (512, 64)])
+def test_quant_bit_exact(gpu, d_nope, d_rope):
+    n = 5000
+    rows = _special_rows(n, d_nope + d_rope, 3)
+    ref = oracle.quant_k_cache(rows[:, :d_nope], rows[:, d_nope:] if d_rope else None)
+    kn = bf16_dev(rows[:, :d_nope], gpu)
+    kr = bf16_dev(rows[:, d_nope:], gpu) if d_rope else None
+    got = dsa.dsa_quant_k_cache(kn, kr).cpu().numpy()
+    assert got.shape == ref.shape
+    bad = np.argwhere(got != ref)
+    assert bad.size == 0, f"{len(bad)} bytes differ, first at {bad[:5].tolist()}"
+
+
+def test_quant_out_loc_strided_and_errors(gpu):
+    n, slots = 700, 2048
+    rows = W.NormalRows(5, 2, n, 300).bits()          # 300-wide source: rows strided, use [:, :256]
+    loc = np.random.default_rng(0).permutation(slots)[:n].astype(np.int64)
+    ref = oracle.quant_k_cache(rows[:, :256], out_loc=loc, num_slots=slots)
+    src = bf16_dev(rows, gpu)[:, :256]
+    cache = torch.zeros((slots, 264), dtype=torch.uint8, device=gpu)
+    err = torch.zeros(1, dtype=torch.int32, device=gpu)
+    dsa.dsa_quant_k_cache(src, out_loc=torch.from_numpy(loc).to(gpu), cache=cache, error_word=err)
+    assert np.array_equal(cache.cpu().numpy(), ref)
+    assert err.item() == 0
+    bad_loc = torch.full((n,), slots, dtype=torch.int64, device=gpu)
+    dsa.dsa_quant_k_cache(src, out_loc=bad_loc, cache=cache, error_word=err)
+    assert err.item() & dsa.DEVERR_SLOT_OUT_OF_RANGE
+    assert np.array_equal(cache.cpu().numpy(), ref)
+
+
+def test_quant_every_e4m3_decision(gpu):
+    """Rows whose quotients x/scale sweep every e4m3 rounding boundary: tiles of 128 values
+    with amax fixed at 448 * 2^k so that x / scale hits exact midpoints and their neighbours."""
+    vals = []
+    pos = sorted(set(abs(oracle.e4m3_value(c)) for c in range(0x7F)))
+    for a, b in zip(pos[:-1], pos[1:]):
+        mid = (a + b) / 2
+        vals += [mid, np.nextafter(np.float32(mid), np.float32(0)), np.nextafter(np.float32(mid), np.float32(500)),
+                 -mid, a, -b]
+    vals = np.array(vals, dtype=np.float32)
+    vals = vals[np.abs(vals) < 448]
+    per = 127
+    n = (len(vals) + per - 1) // per
+    x = np.zeros((n, 256), dtype=np.float32)
+    for i in range(n):
+        chunk = vals[i * per: (i + 1) * per]
+        x[i, : len(chunk)] = chunk
+        x[i, 127] = 448.0                              # amax = 448 -> scale exactly 1
+        x[i, 128:] = x[i, :128] * 2.0 ** -20           # same pattern, scale 2^-20
+    bits = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    ref = oracle.quant_k_cache(bits)
+    got = dsa.dsa_quant_k_cache(bf16_dev(bits, gpu)).cpu().numpy()
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("kind,d_nope,d_rope", [(1, 256, 0), (1, 512, 64), (0, 256, 0), (0, 512, 64)])
+def test_gather_dequant_bit_exact(gpu, kind, d_nope, d_rope):
+    slots = 3000
+    D = d_nope + d_rope
+    rows = _special_rows(slots, D, 7)
+    cache = rows if kind == 0 else oracle.quant_k_cache(rows[:, :d_nope], rows[:, d_nope:] if d_rope else None)
+    rng = np.random.default_rng(1)
+    idx = rng.integers(-2, slots, size=4000).astype(np.int32)
+    ref, bad = oracle.gather_dequant(cache, kind, d_nope, d_rope, idx)
+    assert bad == 0
+    dcache = bf16_dev(cache, gpu) if kind == 0 else torch.from_numpy(cache).to(gpu)
+    got = dsa.dsa_gather_dequant(dcache, kind, d_nope, d_rope, torch.from_numpy(idx).to(gpu))
+    assert np.array_equal(bits_of(got), ref)
+
+
+def test_gather_dequant_paged_repeated_pages_and_errors(gpu):
+    ps, pages = 64, 40
+    slots = ps * pages
+    rows = W.NormalRows(9, 3, slots, 256).bits()
+    cache = oracle.quant_k_cache(rows)
+    rng = np.random.default_rng(2)
+    bt = rng.integers(0, pages, size=(3, 12)).astype(np.int32)       # repeated physical pages
+    bt[1, :] = 7                                                      # every logical page -> page 7
+    idx = rng.integers(-1, 12 * ps, size=3000).astype(np.int32)
+    req = rng.integers(0, 3, size=3000).astype(np.int32)
+    ref, bad = oracle.gather_dequant(cache, 1, 256, 0, idx, block_table=bt, page_size=ps, req_of_index=req)
+    assert bad == 0
+    dcache = torch.from_numpy(cache).to(gpu)
+    got = dsa.dsa_gather_dequant(dcache, 1, 256, 0, torch.from_numpy(idx).to(gpu),
+                                 block_table=torch.from_numpy(bt).to(gpu), page_size=ps,
+                                 req_of_index=torch.from_numpy(req).to(gpu))
+    assert np.array_equal(bits_of(got), ref)
+    # out-of-range logical positions / slots: zero rows and the error bit
+    err = torch.zeros(1, dtype=torch.int32, device=gpu)
+    oob = torch.tensor([12 * ps, 3, 10 ** 6], dtype=torch.int32, device=gpu)
+    got = dsa.dsa_gather_dequant(dcache, 1, 256, 0, oob, block_table=torch.from_numpy(bt).to(gpu), page_size=ps,
+                                 error_word=err)
+    assert err.item() & dsa.DEVERR_INDEX_OUT_OF_RANGE
+    g = bits_of(got)
+    assert (g[0] == 0).all() and (g[2] == 0).all() and (g[1] != 0).any()
+
+
+def test_pack_then_gather_round_trip_on_gpu_matches_oracle(gpu):
+    """GPU pack followed by GPU gather equals the oracle's pack + gather (256+0 and 512+64)."""
+    for d_nope, d_rope in [(256, 0), (512, 64)]:
+        rows = W.NormalRows(11, 4, 1000, d_nope + d_rope).bits()
+        ref_cache = oracle.quant_k_cache(rows[:, :d_nope], rows[:, d_nope:] if d_rope else None)
+        idx = np.arange(999, -1, -1, dtype=np.int32)
+        ref, _ = oracle.gather_dequant(ref_cache, 1, d_nope, d_rope, idx)
+        c = dsa.dsa_quant_k_cache(bf16_dev(rows[:, :d_nope], gpu), bf16_dev(rows[:, d_nope:], gpu) if d_rope else None)
+        got = dsa.dsa_gather_dequant(c, 1, d_nope, d_rope, torch.from_numpy(idx).to(gpu))
+        assert np.array_equal(bits_of(got), ref)
