@@ -1,0 +1,363 @@
+"""Benchmark: DSA sparse MLA attention on one GB300 (or N independent replicas).
+
+Default workload: batched decode over a packed scaled-FP8 paged cache, 256+0 latent geometry,
+256 requests x 32768 positions (8,388,608 slots, 2.2 GB of 264-byte rows), one query token per
+request, top-k 2048 valid entries per token in a 2112-wide list (70% from the last 4096
+positions, 30% uniform over the rest; 5% of tokens with the -1 padding scattered), 64 heads,
+sm_scale 1/16. One step = one dsa_sparse_attn call over the whole batch.
+
+Prints ONE JSON line (rank 0). Timing: W untimed warm-up steps, then K timed steps; every step is
+bracketed by CUDA events on the launching stream and a 512 MB buffer is written between steps
+(outside the events) so the L2 (129 MB) holds none of the step's inputs. ``value`` = tokens per
+second over the K steps (all ranks, max time over ranks). ``e2e`` repeats the measurement through
+the same call with the step's inputs (q, indices) copied from pinned host memory and the output
+copied back inside the timed region. ``cpu_baseline`` times the CPU oracle on a bounded sample.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_FLUSH_BYTES = 512 << 20
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def algorithmic_work(wl):
+    """Algorithmic bytes and FLOPs of one full call (per the data each token must touch once):
+    gathered rows (valid entries x row bytes) + q + out + the index list + the block table;
+    FLOPs = 2 * H * n_valid * (D_K + d_v)."""
+    n_valid = int((wl.indices >= 0).sum())
+    rb = (wl.d_nope + 4 * (wl.d_nope // 128) + 2 * wl.d_rope) if wl.kind == 1 else 2 * wl.D
+    rows = n_valid * rb
+    q = wl.T * wl.H * wl.D * 2
+    out = wl.T * wl.H * wl.d_v * 2
+    idx = wl.indices.size * 4
+    bt = 0 if wl.block_table is None else wl.block_table.size * 4
+    flops = 2.0 * wl.H * n_valid * (wl.D + wl.d_v)
+    return {"bytes": rows + q + out + idx + bt, "row_bytes": rows, "flops": flops, "n_valid": n_valid}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        import torch
+
+        try:
+            self.gpu_id = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+        except Exception:
+            self.gpu_id = str(device.index or 0)
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, pw, reasons = [], None, [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+                pw.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(pw) if pw else None}
+
+
+# ------------------------------------------------------------------------------ GPU inputs --
+def build_device_inputs(wl, device):
+    """Resident inputs for one workload: the cache is generated and packed on the GPU."""
+    import torch
+
+    import dsa_sparse_attention_mla_gb300 as dsa
+
+    q = wl.q.torch(device).view(wl.T, wl.H, wl.D)
+    if wl.kind == 0:
+        cache = wl.kv.torch(device)
+    else:
+        rb = dsa.dsa_packed_row_bytes(wl.d_nope, wl.d_rope)
+        cache = torch.empty((wl.num_slots, rb), dtype=torch.uint8, device=device)
+        chunk = 1 << 20
+        loc_all = None if wl.kv_slot is None else torch.from_numpy(wl.kv_slot).to(device)
+        from dsa_sparse_attention_mla_gb300.workloads import normal_bf16_torch
+
+        for r0 in range(0, wl.num_slots, chunk):
+            n = min(chunk, wl.num_slots - r0)
+            rows = normal_bf16_torch(wl.kv.seed, wl.kv.stream, r0 * wl.D, n * wl.D, device).view(n, wl.D)
+            loc = (torch.arange(r0, r0 + n, device=device, dtype=torch.int64) if loc_all is None else loc_all[r0:r0 + n])
+            dsa.dsa_quant_k_cache(rows[:, : wl.d_nope], rows[:, wl.d_nope:] if wl.d_rope else None, out_loc=loc,
+                                  cache=cache, num_slots=wl.num_slots)
+        torch.cuda.synchronize(device)
+    idx = torch.from_numpy(wl.indices).to(device)
+    bt = None if wl.block_table is None else torch.from_numpy(wl.block_table).to(device)
+    req = None if wl.req_of_token is None else torch.from_numpy(wl.req_of_token).to(device)
+    return q, cache, idx, bt, req
+
+
+def run_gpu(args, wl, rank, world, device):
+    import torch
+
+    import dsa_sparse_attention_mla_gb300 as dsa
+
+    q, cache, idx, bt, req = build_device_inputs(wl, device)
+    out = torch.empty((wl.T, wl.H, wl.d_v), dtype=torch.bfloat16, device=device)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    ws = torch.zeros(dsa.dsa_sparse_attn_workspace_size(wl.d_v), dtype=torch.uint8, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(o=out, qq=q, ii=idx):
+        dsa.dsa_sparse_attn(qq, cache, wl.kind, ii, wl.sm_scale, d_nope=wl.d_nope, d_rope=wl.d_rope, d_v=wl.d_v,
+                            block_table=bt, page_size=wl.page_size, req_of_token=req, out=o, workspace=ws,
+                            error_word=err)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize(device)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    with ClockSampler(device) as clk:
+        t_wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(device)
+        t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        torch.distributed.barrier()
+    times = [s.elapsed_time(e) for s, e in zip(starts, ends)]  # ms
+    total_ms = float(sum(times))
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    if err.item() != 0:
+        raise RuntimeError(f"device error word {err.item()} during the benchmark")
+
+    # ---- end to end: host-resident q and indices in, output back to host, copies timed
+    e2e_steps = max(3, min(args.steps, 200))
+    q_h = q.cpu().pin_memory()
+    idx_h = idx.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    q_d, idx_d = torch.empty_like(q), torch.empty_like(idx)
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    for i in range(e2e_steps + 2):
+        flush.fill_(3)
+        if i >= 2:
+            e_s[i - 2].record(stream)
+        q_d.copy_(q_h, non_blocking=True)
+        idx_d.copy_(idx_h, non_blocking=True)
+        step(out, q_d, idx_d)
+        out_h.copy_(out, non_blocking=True)
+        if i >= 2:
+            e_e[i - 2].record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = float(sum(s.elapsed_time(e) for s, e in zip(e_s, e_e)) / e2e_steps)
+    h2d = q.numel() * q.element_size() + idx.numel() * idx.element_size()
+    d2h = out.numel() * out.element_size()
+    return {"total_ms": total_ms, "times": times, "t_wall": t_wall, "clocks": clk.summary(), "e2e_ms": e2e_ms,
+            "h2d": h2d, "d2h": d2h}
+
+
+# ---------------------------------------------------------------------------- CPU oracle --
+class OracleRunner:
+    """The CPU oracle (as it stands) on the workload. The packed cache rows the tokens name are
+    generated and packed by the oracle on the host: no oracle input comes from the GPU path."""
+
+    def __init__(self, wl):
+        import oracle
+
+        sys.path.insert(0, os.path.join(ROOT, "tests"))
+        from _helpers import oracle_cache, slots_of_tokens  # noqa: E402
+
+        self.oracle = oracle
+        self.wl = wl
+        self.q = wl.q_bits()
+        self.cache = oracle_cache(wl, rows=_kv_rows_for(wl, slots_of_tokens(wl, np.arange(wl.T))))
+        self.order = np.random.default_rng(1234).permutation(wl.T)
+        self.threads = oracle.max_threads()
+
+    def run(self, tokens) -> float:
+        wl = self.wl
+        t0 = time.perf_counter()
+        self.oracle.sparse_attn(self.q, self.cache, wl.kind, wl.d_nope, wl.d_rope, wl.d_v, wl.indices, wl.sm_scale,
+                                block_table=wl.block_table, page_size=wl.page_size, req_of_token=wl.req_of_token,
+                                tokens=np.asarray(tokens, dtype=np.int64))
+        return time.perf_counter() - t0
+
+    def sample(self, seconds: float):
+        """tokens/s on a bounded sample sized to about ``seconds`` of host time."""
+        probe = self.order[: min(self.wl.T, max(self.threads, 8))]
+        per_tok = self.run(probe) / len(probe)
+        n = int(min(self.wl.T, max(len(probe), seconds / max(per_tok, 1e-9))))
+        dt = self.run(self.order[:n])
+        return n / dt, min(self.threads, n), f"{n} of {self.wl.T} tokens (seeded random subset), full top-k lists"
+
+
+def _kv_rows_for(wl, slots):
+    """kv row ids whose packed row lands in the given physical slots."""
+    if wl.kv_slot is None:
+        return slots
+    inv = np.empty(wl.num_slots, dtype=np.int64)
+    inv[wl.kv_slot] = np.arange(wl.num_slots)
+    return inv[slots]
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    from dsa_sparse_attention_mla_gb300 import workloads as W
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    wl = W.config(args.config, seed=0)
+    work = algorithmic_work(wl)
+    metric = "sparse-attn tokens/s (256+0 FP8, T=256)" if args.config == 3 else f"sparse-attn tokens/s ({wl.name})"
+    cfg = {"workload": wl.name, "tokens_per_step": wl.T, "heads": wl.H, "d_nope": wl.d_nope, "d_rope": wl.d_rope,
+           "d_v": wl.d_v, "topk": wl.topk, "valid_entries": work["n_valid"], "cache": "fp8_264B" if wl.kind else "bf16",
+           "slots": wl.num_slots, "page_size": wl.page_size or None,
+           "l2": f"{L2_FLUSH_BYTES >> 20} MB buffer written between timed steps (outside the events)"}
+
+    if args.impl == "reference":
+        # The reference arm is the CPU oracle as it stands, on rank 0 only; each step runs a
+        # bounded sample of the workload's tokens so the whole run stays within a few minutes.
+        if rank != 0:
+            return
+        runner = OracleRunner(wl)
+        per_tok = runner.run(runner.order[:1])
+        budget = 150.0
+        n = int(max(1, min(wl.T, budget / ((args.steps + args.warmup) * max(per_tok, 1e-9)))))
+        tot_t, tot_n = 0.0, 0
+        for i in range(args.warmup + args.steps):
+            toks = np.roll(runner.order, -i * n)[:n]
+            dt = runner.run(toks)
+            if i >= args.warmup:
+                tot_t += dt
+                tot_n += n
+        v = tot_n / tot_t
+        cores = min(runner.threads, n)
+        sample = f"{n} of {wl.T} tokens per step (seeded rotation), full top-k lists"
+        line = {"impl": "reference", "metric": metric, "value": v, "unit": "tokens/s", "n_gpus": 0,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * wl.T / v,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": cfg,
+                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+                "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    device = torch.device("cuda", local_rank)
+    import __graft_entry__
+
+    __graft_entry__.build() if rank == 0 else None
+    if world > 1:
+        torch.distributed.barrier()
+    r = run_gpu(args, wl, rank, world, device)
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    hbm, bf16, bf16_sus, peak_src = _peaks()
+    ms_per_step = r["total_ms"] / args.steps
+    value = world * wl.T * args.steps / (r["total_ms"] / 1000.0)
+    achieved = work["bytes"] / (ms_per_step / 1000.0) / 1e9
+    tflops = work["flops"] / (ms_per_step / 1000.0) / 1e12
+    cpu_v, cores, sample = OracleRunner(wl).sample(args.cpu_seconds)
+    line = {
+        "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": None, "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": work["bytes"], "tflops": tflops,
+                     "tensor_frac_of_bf16_burst": tflops / bf16},
+        "cpu_baseline": {"value": cpu_v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": world * wl.T / (r["e2e_ms"] / 1000.0), "unit": "tokens/s", "h2d_bytes_per_step": r["h2d"],
+                "d2h_bytes_per_step": r["d2h"]},
+        "gpu_launches": args.steps,
+        "clocks": r["clocks"],
+        "step_ms": {"median": statistics.median(r["times"]), "min": min(r["times"]), "max": max(r["times"])},
+    }
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -15,10 +15,11 @@
 //    into equal contiguous ranges, one per CTA ("stream-K"); a token cut by a range boundary
 //    is finished by the CTA holding its first tiles, which merges the other CTAs' partial
 //    (o, max, sum) from the workspace in a fixed order (deterministic, no atomics on data).
-//  * Warp roles: warp 0 producer (index read, -1 compaction, page translation, TMA gathers
-//    for bf16 rows / L2 prefetch for FP8 rows, Q loads), warp 1 MMA issuer, warps 4-7 softmax
-//    + epilogue (one per TMEM sub-partition, 16 heads each), warps 8-15 (FP8 only) dequant:
-//    they load packed rows and write bf16(code * scale) into the 128-byte-swizzled K tile.
+//  * Warp roles: warp 0 producer (index read, -1 compaction, page translation, L2 prefetch of
+//    index / block-table / FP8 rows, Q loads by TMA), warp 1 MMA issuer, warps 4-7 softmax +
+//    epilogue (one per TMEM sub-partition, 16 heads each), warps 8-15 row loaders: cp.async
+//    16-byte copies of bf16 rows, or loads of packed FP8 rows widened to bf16(code * scale),
+//    into the 128-byte-swizzled K-major tile.
 //  * Online softmax in the exp2 domain with a lazy rescale (O and the running sum are only
 //    rescaled when the running max grows by more than 2^8), zero-RoPE work compiled out.
 #include <cuda.h>
@@ -42,13 +43,13 @@ struct AttnCfg {
   static constexpr int DVC = 256;                  // output columns per CTA pass
   static constexpr int BN = BN_;                   // gathered keys per tile (MMA N of S)
   static constexpr int KSTAGES = KSTAGES_;
-  static constexpr int MSTAGES = 4;
+  static constexpr int MSTAGES = DK > 256 ? 4 : 8;  // meta ring depth (smem-limited for 512+64)
   static constexpr int KCH = DK / 64;              // 128-byte chunks along d
   static constexpr int PCH = (BN + 63) / 64;       // 128-byte chunks of P along keys
   static constexpr int HALF = BN / 2;              // keys per softmax thread
   static constexpr int RB = D_NOPE + 4 * (D_NOPE / 128) + 2 * D_ROPE;
   static constexpr int ROWB = KIND == DSA_CACHE_BF16 ? 2 * DK : RB;  // cache row bytes
-  static constexpr int NDEQ = KIND == DSA_CACHE_FP8_SCALED ? 8 : 0;
+  static constexpr int NDEQ = 8;                   // loader warps (cp.async rows / FP8 dequant)
   static constexpr int WARPS = 8 + NDEQ;
   static constexpr int THREADS = 32 * WARPS;
   static constexpr int IDX_PER_LANE = (BN + 31) / 32;
@@ -125,8 +126,7 @@ __device__ __forceinline__ int64_t unit_begin(int64_t b, int64_t U, int G) { ret
 // ------------------------------------------------------------------------------ kernel --
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
-    dsa_attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmap_q,
-                    const __grid_constant__ CUtensorMap tmap_kv) {
+    dsa_attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmap_q) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -151,12 +151,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     for (int s = 0; s < C::KSTAGES; ++s) {
-      mbar_init(k_full(s), C::KIND == DSA_CACHE_BF16 ? 1 : C::NDEQ);
+      // bf16 rows: one cp.async arrive per loader thread; FP8 rows: one arrive per loader warp
+      mbar_init(k_full(s), C::KIND == DSA_CACHE_BF16 ? 32 * C::NDEQ : C::NDEQ);
       mbar_init(k_empty(s), 1);
     }
     for (int s = 0; s < C::MSTAGES; ++s) {
       mbar_init(m_full(s), 1);
-      mbar_init(m_empty(s), 1 + 4 + C::NDEQ);
+      mbar_init(m_empty(s), 1 + 2 + 4 + C::NDEQ);  // MMA thread, 2 prefetch, 4 softmax, loader warps
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(s_full(b), 1);
@@ -171,10 +172,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tmap_q);
-    if (C::KIND == DSA_CACHE_BF16) prefetch_tmap(&tmap_kv);
-  }
+  if (warp == 0 && lane == 0) prefetch_tmap(&tmap_q);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -193,7 +191,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
   if (warp == 0) {
     // =========================================================== producer (one warp) ====
-    uint32_t mc = 0, g = 0, qc = 0;
+    // Walks this CTA's unit range segment by segment. Per key tile it reads the tile's index
+    // window, masks entries < 0, translates logical positions through the block table, and
+    // emits a meta entry with the compacted slot list. The index loads run two tiles ahead and
+    // the block-table loads one tile ahead, so a tile (or a run of empty tiles) costs no
+    // round trip of its own; both index rows and block-table rows are pulled into L2 at the
+    // segment start, and FP8 rows into L2 as soon as their slot is known.
+    uint32_t mc = 0, qc = 0;
     const int64_t u0 = unit_begin(b, p.U, p.G), u1 = unit_begin(b + 1, p.U, p.G);
     auto emit_begin = [&](int& st) -> MetaHdr* {
       st = mc % C::MSTAGES;
@@ -205,6 +209,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       if (lane == 0) mbar_arrive(m_full(st));
       ++mc;
     };
+    constexpr int IPL = C::IDX_PER_LANE;
+    const int64_t pos_limit = p.bt ? (int64_t)p.max_pages * p.page_size : p.num_slots;
     int64_t u = u0;
     while (u < u1 && !*abort_flag) {
       const int64_t vt = u / p.NT;
@@ -215,46 +221,52 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       const int kind = j0 > 0 ? kPart : (j1 < p.NT ? kHead : kComplete);
       const int64_t req = p.req ? p.req[t] : 0;
       const int32_t* irow = p.idx + t * p.idx_stride;
-      bool had = false;
-      for (int j = j0; j < j1 && !*abort_flag; ++j) {
-        // --- read this tile's index window, mask, translate, compact
-        int slot_k[C::IDX_PER_LANE];
-        bool ok_k[C::IDX_PER_LANE];
-        int bad = 0;
-#pragma unroll
-        for (int k = 0; k < C::IDX_PER_LANE; ++k) {
-          const int e = j * C::BN + 32 * k + lane;
-          ok_k[k] = false;
-          slot_k[k] = 0;
-          if (32 * k + lane < C::BN && e < p.topk) {
-            const int64_t pos = irow[e];
-            if (pos >= 0) {
-              int64_t slot;
-              if (!p.bt) {
-                slot = pos < p.num_slots ? pos : -2;
-              } else if (pos >= (int64_t)p.max_pages * p.page_size) {
-                slot = -2;
-              } else {
-                const int64_t page = p.bt[req * p.bt_stride + pos / p.page_size];
-                slot = page < 0 ? -2 : page * p.page_size + pos % p.page_size;
-                if (slot >= p.num_slots) slot = -2;
-              }
-              if (slot >= 0) {
-                ok_k[k] = true;
-                slot_k[k] = (int)slot;
-              } else {
-                bad = 1;
-              }
-            }
-          }
+      const int32_t* btrow = p.bt ? p.bt + req * p.bt_stride : nullptr;
+      {  // pull this segment's index window and the request's block-table row into L2
+        const int e0 = j0 * C::BN, e1 = min(j1 * C::BN, p.topk);
+        const uintptr_t a0 = reinterpret_cast<uintptr_t>(irow + e0) & ~uintptr_t(127);
+        const uintptr_t a1 = reinterpret_cast<uintptr_t>(irow + e1);
+        for (uintptr_t a = a0 + 128 * lane; a < a1; a += 32 * 128)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+        if (btrow) {
+          const uintptr_t c0 = reinterpret_cast<uintptr_t>(btrow) & ~uintptr_t(127);
+          const uintptr_t c1 = reinterpret_cast<uintptr_t>(btrow + p.max_pages);
+          for (uintptr_t a = c0 + 128 * lane; a < c1; a += 32 * 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
         }
-        if (bad) set_err(p.err, DSA_DEVERR_INDEX_OUT_OF_RANGE);
-        int n_valid = 0;
+      }
+      // The segment's index window [e0, e1) is read 256 entries per step (entry pos + 32k + lane
+      // in lane `lane`, slot k). Index loads run two steps ahead and block-table loads one step
+      // ahead. Valid entries are packed, in index order, into dense tiles of BN rows, so runs of
+      // -1 padding cost only their index reads and every emitted tile but the segment's last
+      // is full.
+      constexpr int V = 8;
+      const int e0 = j0 * C::BN, e1 = min(j1 * C::BN, p.topk);
+      auto load_step = [&](int pos, int (&v)[V]) {
 #pragma unroll
-        for (int k = 0; k < C::IDX_PER_LANE; ++k) n_valid += __popc(__ballot_sync(0xffffffffu, ok_k[k]));
-        if (n_valid == 0) continue;
-        // --- Q of this segment (first non-empty tile)
-        if (!had) {
+        for (int k = 0; k < V; ++k) {
+          const int e = pos + 32 * k + lane;
+          v[k] = e < e1 ? __ldg(irow + e) : -1;
+        }
+      };
+      auto page_of = [&](const int (&x)[V], int (&pg)[V]) {
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+          if (x[k] < 0) pg[k] = -1;
+          else if (x[k] >= pos_limit) pg[k] = -2;
+          else pg[k] = btrow ? __ldg(btrow + x[k] / p.page_size) : x[k];
+        }
+      };
+      int ia[V], ib[V], pa[V];
+      load_step(e0, ia);
+      load_step(e0 + 32 * V, ib);
+      page_of(ia, pa);
+      bool had = false, open = false;
+      int cnt = 0, st = 0;
+      int* slots = nullptr;
+      MetaHdr* mh = nullptr;
+      auto open_tile = [&]() {
+        if (!had) {  // Q of this segment, loaded with its first tile
           if (qc > 0) wait(q_empty, (qc - 1) & 1);
           if (lane == 0) mbar_arrive_expect_tx(q_full, C::Q_BYTES);
           __syncwarp();
@@ -262,59 +274,69 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             tma_load_3d(sbase + C::Q_OFF + lane * (kHeads * 128), &tmap_q, 64 * lane, 0, (int)t, q_full);
           ++qc;
         }
-        // --- meta entry with the compacted slot list
-        int st;
-        MetaHdr* mh = emit_begin(st);
-        int* slots = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(mh) + 32);
-        int cnt = 0;
-#pragma unroll
-        for (int k = 0; k < C::IDX_PER_LANE; ++k) {
-          const uint32_t bal = __ballot_sync(0xffffffffu, ok_k[k]);
-          if (ok_k[k]) {
-            const int pos = cnt + __popc(bal & ((1u << lane) - 1u));
-            slots[pos] = slot_k[k];
-            if constexpr (C::KIND == DSA_CACHE_FP8_SCALED) {
-              // pull the packed row into L2 ahead of the dequant warps' loads
-              const uint8_t* row = p.cache + (int64_t)slot_k[k] * C::RB;
-              const uintptr_t a = reinterpret_cast<uintptr_t>(row);
-              const uintptr_t a0 = a & ~uintptr_t(15);
-              uint32_t sz = (uint32_t)(((a + C::RB + 15) & ~uintptr_t(15)) - a0);
-              const uintptr_t end = reinterpret_cast<uintptr_t>(p.cache) + (uintptr_t)p.num_slots * C::RB;
-              if (a0 + sz > end) sz = (uint32_t)((end - a0) & ~uintptr_t(15));
-              if (sz > 0)
-                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a0), "r"(sz) : "memory");
-            }
-          }
-          cnt += __popc(bal);
-        }
+        mh = emit_begin(st);
+        slots = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(mh) + 32);
         if (lane == 0) {
           mh->type = kTile;
           mh->vtoken = (int)vt;
-          mh->n_valid = n_valid;
           mh->first = had ? 0 : 1;
         }
         had = true;
+        open = true;
+        cnt = 0;
+      };
+      auto close_tile = [&](int n) {
+        if (lane == 0) mh->n_valid = n;
         emit_end(st);
-        // --- bf16 rows: TMA gather straight into the swizzled K tile
-        if constexpr (C::KIND == DSA_CACHE_BF16) {
-          const int ks = g % C::KSTAGES;
-          if (g >= (uint32_t)C::KSTAGES) wait(k_empty(ks), ((g / C::KSTAGES) & 1) ^ 1);
-          if (lane == 0) mbar_arrive_expect_tx(k_full(ks), C::KT_BYTES);
-          __syncwarp();
-          const uint32_t kt = sbase + C::KT_OFF + ks * C::KT_BYTES;
-          const int oob = (int)p.num_slots;  // rows past n_valid read out of bounds -> zeros
-          for (int w = lane; w < (C::BN / 4) * C::KCH; w += 32) {
-            const int q4 = w % (C::BN / 4), c = w / (C::BN / 4);
-            const int r = 4 * q4;
-            const int s0 = r + 0 < n_valid ? slots[r + 0] : oob;
-            const int s1 = r + 1 < n_valid ? slots[r + 1] : oob;
-            const int s2 = r + 2 < n_valid ? slots[r + 2] : oob;
-            const int s3 = r + 3 < n_valid ? slots[r + 3] : oob;
-            tma_gather4(kt + c * (C::BN * 128) + r * 128, &tmap_kv, 64 * c, s0, s1, s2, s3, k_full(ks));
+        open = false;
+      };
+      for (int pos = e0; pos < e1 && !*abort_flag; pos += 32 * V) {
+        int ic[V], pb[V];
+        load_step(pos + 64 * V, ic);
+        page_of(ib, pb);
+        int bad = 0;
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+          int64_t slot = -1;
+          if (pa[k] >= 0) {
+            if (btrow) {
+              slot = (int64_t)pa[k] * p.page_size + ia[k] % p.page_size;
+              if (slot >= p.num_slots) slot = -2;
+            } else {
+              slot = pa[k];
+            }
+          } else if (pa[k] == -2 || (btrow && ia[k] >= 0)) {
+            slot = -2;  // outside the addressable range, or a negative block-table page
+          }
+          bad |= (slot == -2);
+          const bool ok = slot >= 0;
+          const uint32_t bal = __ballot_sync(0xffffffffu, ok);
+          if (bal == 0u) continue;
+          if (!open) open_tile();
+          const int n = __popc(bal);
+          const int my = cnt + __popc(bal & ((1u << lane) - 1u));
+          if (ok && my < C::BN) slots[my] = (int)slot;
+          if (cnt + n >= C::BN) {  // this group fills the tile (and may spill into the next one)
+            close_tile(C::BN);
+            const int rest = cnt + n - C::BN;
+            if (rest > 0) {
+              open_tile();
+              if (ok && my >= C::BN) slots[my - C::BN] = (int)slot;
+              cnt = rest;
+            }
+          } else {
+            cnt += n;
           }
         }
-        ++g;
+        if (bad) set_err(p.err, DSA_DEVERR_INDEX_OUT_OF_RANGE);
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+          ia[k] = ib[k];
+          ib[k] = ic[k];
+          pa[k] = pb[k];
+        }
       }
+      if (open) close_tile(cnt);
       {
         int st;
         MetaHdr* mh = emit_begin(st);
@@ -347,16 +369,21 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       constexpr uint32_t idPV = idesc_bf16(64, C::DVC, 0, 1);
       uint32_t mc = 0, g = 0, qc = 0;
       int pend = -1, pend_first = 0, pend_dvh = 0;
+      // Descriptors are built once; the k-step offsets are compile-time adds on the 16-byte
+      // address field (every operand stays below 256 KB of shared memory).
+      const uint64_t dQ = sw128_desc(sbase + C::Q_OFF, 16, 1024);
+      const uint64_t dP = sw128_desc(sbase + C::P_OFF, 16, 1024);
       auto issue_pv = [&](uint32_t gg, int first, int dvh) {
         if (!wait(p_full, gg & 1)) return;
         tc_fence_after();
         const int ks = gg % C::KSTAGES;
-        const uint32_t vbase = sbase + C::KT_OFF + ks * C::KT_BYTES + dvh * (C::DVC / 64) * (C::BN * 128);
+        const uint64_t dV = sw128_desc(sbase + C::KT_OFF + ks * C::KT_BYTES + dvh * (C::DVC / 64) * (C::BN * 128),
+                                       C::BN * 128, 1024);
+#pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk) {
-          const uint32_t pa = sbase + C::P_OFF + (kk >> 2) * (kHeads * 128) + (kk & 3) * 32;
-          const uint64_t ad = sw128_desc(pa, 16, 1024);
-          const uint64_t bd = sw128_desc(vbase + kk * 16 * 128, C::BN * 128, 1024);
-          mma_bf16(tmem + C::O_COL, ad, bd, idPV, (first && kk == 0) ? 0u : 1u);
+          const uint64_t pa = (uint64_t)(((kk >> 2) * (kHeads * 128) + (kk & 3) * 32) >> 4);
+          const uint64_t vb = (uint64_t)((kk * 16 * 128) >> 4);
+          mma_bf16(tmem + C::O_COL, dP + pa, dV + vb, idPV, (first && kk == 0) ? 0u : 1u);
         }
         mma_commit(k_empty(ks));
         mma_commit(pv_done);
@@ -377,13 +404,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           const int ks = g % C::KSTAGES;
           if (!wait(k_full(ks), (g / C::KSTAGES) & 1)) break;
           if (g >= 2 && !wait(s_empty(g & 1), ((g >> 1) & 1) ^ 1)) break;
+          // bf16 rows arrive by cp.async, i.e. through the generic proxy: order them before the
+          // tensor core reads (the FP8 loaders fence on their side before arriving)
+          if constexpr (C::KIND == DSA_CACHE_BF16) fence_proxy_async_smem();
           tc_fence_after();
-          const uint32_t kbase = sbase + C::KT_OFF + ks * C::KT_BYTES;
+          const uint64_t dK = sw128_desc(sbase + C::KT_OFF + ks * C::KT_BYTES, 16, 1024);
+#pragma unroll
           for (int kk = 0; kk < C::DK / 16; ++kk) {
-            const uint32_t qa = sbase + C::Q_OFF + (kk >> 2) * (kHeads * 128) + (kk & 3) * 32;
-            const uint32_t ka = kbase + (kk >> 2) * (C::BN * 128) + (kk & 3) * 32;
-            mma_bf16(tmem + C::S_COL + (g & 1) * C::BN, sw128_desc(qa, 16, 1024), sw128_desc(ka, 16, 1024), idS,
-                     kk > 0 ? 1u : 0u);
+            const uint64_t qa = (uint64_t)(((kk >> 2) * (kHeads * 128) + (kk & 3) * 32) >> 4);
+            const uint64_t ka = (uint64_t)(((kk >> 2) * (C::BN * 128) + (kk & 3) * 32) >> 4);
+            mma_bf16(tmem + C::S_COL + (g & 1) * C::BN, dQ + qa, dK + ka, idS, kk > 0 ? 1u : 0u);
           }
           mma_commit(s_full(g & 1));
           if (pend >= 0) issue_pv((uint32_t)pend, pend_first, pend_dvh);
@@ -395,6 +425,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           const int had = mh->had_tiles;
           mbar_arrive(m_empty(st));
           if (had) mma_commit(q_empty);
+          // finish the segment's last PV now rather than after the next segment's first S, so
+          // the epilogue does not wait for the next Q load
+          if (pend >= 0) {
+            issue_pv((uint32_t)pend, pend_first, pend_dvh);
+            pend = -1;
+          }
         } else {
           mbar_arrive(m_empty(st));
           ++mc;
@@ -407,6 +443,33 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       if (g > 0) mbar_wait(pv_done, (g - 1) & 1);
     }
     __syncwarp();
+  } else if (warp == 2 || warp == 3) {
+    // ========================================================= L2 prefetch (2 warps) ====
+    // Packed FP8 rows are pulled into L2 as soon as their tile's slot list is published, a
+    // few tiles before the loader warps read them. One LSU prefetch per 128-byte line.
+    uint32_t mc = 0;
+    const int pl = (warp - 2) * 32 + lane;  // 0..63
+    while (!*abort_flag) {
+      const int st = mc % C::MSTAGES;
+      if (!wait(m_full(st), (mc / C::MSTAGES) & 1)) break;
+      const MetaHdr* mh = reinterpret_cast<const MetaHdr*>(smem + C::META_OFF + st * C::META_BYTES);
+      const int type = mh->type;
+      if constexpr (C::KIND == DSA_CACHE_FP8_SCALED) {
+        if (type == kTile) {
+          const int n_valid = mh->n_valid;
+          const int* slots = reinterpret_cast<const int*>(reinterpret_cast<const uint8_t*>(mh) + 32);
+          for (int r = pl; r < n_valid; r += 64) {
+            const uintptr_t r0 = reinterpret_cast<uintptr_t>(p.cache + (int64_t)slots[r] * C::RB);
+            for (uintptr_t a = r0 & ~uintptr_t(127); a < r0 + C::RB; a += 128)
+              asm volatile("prefetch.global.L2 [%0];" ::"l"(a > r0 ? a : r0));
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(m_empty(st));
+      ++mc;
+      if (type == kDone) break;
+    }
   } else if (warp >= 4 && warp < 8) {
     // =============================================== softmax + epilogue (4 warps) ====
     const int sp = warp & 3;                 // TMEM sub-partition
@@ -440,58 +503,67 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         float s[C::HALF];
         {
           const uint32_t ta = trow + C::S_COL + (g & 1) * C::BN;
-          uint32_t r[32];
+          uint32_t r[C::HALF];
+          // all column chunks of this thread's key half, then a single wait
 #pragma unroll
-          for (int c0 = 0; c0 < C::HALF; c0 += 32) {
-            if (c0 + 32 <= C::HALF) {
-              tmem_ld16x2_x32<C::HALF>(ta + c0, r);
-            } else {
-              // HALF not a multiple of 32: the last 24 / 16 / 8 columns
-              if constexpr (C::HALF % 32 == 24) {
-                tmem_ld16x2_x16<C::HALF>(ta + c0, r);
-                tmem_ld16x2_x8<C::HALF>(ta + c0 + 16, r + 16);
-              } else if constexpr (C::HALF % 32 == 16) {
-                tmem_ld16x2_x16<C::HALF>(ta + c0, r);
-              } else if constexpr (C::HALF % 32 == 8) {
-                tmem_ld16x2_x8<C::HALF>(ta + c0, r);
-              }
-            }
-            tc_wait_ld();
+          for (int c0 = 0; c0 + 32 <= C::HALF; c0 += 32)
+            tmem_ld16x2_x32<C::HALF>(ta + c0, *reinterpret_cast<uint32_t(*)[32]>(r + c0));
+          constexpr int TAIL = C::HALF % 32, T0 = C::HALF - TAIL;
+          if constexpr (TAIL >= 16) tmem_ld16x2_x16<C::HALF>(ta + T0, r + T0);
+          if constexpr (TAIL % 16 == 8) tmem_ld16x2_x8<C::HALF>(ta + T0 + (TAIL & 16), r + T0 + (TAIL & 16));
+          tc_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (c0 + i < C::HALF) s[c0 + i] = __uint_as_float(r[i]);
-          }
+          for (int i = 0; i < C::HALF; ++i) s[i] = __uint_as_float(r[i]);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(s_empty(g & 1));
-        // mask and row max (the two threads of a head hold its two key halves)
+        // mask keys past n_valid (only a partially filled tile has any), then the row max with
+        // four independent chains; the two threads of a head hold its two key halves
         const int kbase = hf * C::HALF;
-        float mx = -INFINITY;
+        if (n_valid < C::BN) {
 #pragma unroll
-        for (int i = 0; i < C::HALF; ++i) {
-          if (kbase + i >= n_valid) s[i] = -INFINITY;
-          mx = fmaxf(mx, s[i]);
+          for (int i = 0; i < C::HALF; ++i)
+            if (kbase + i >= n_valid) s[i] = -INFINITY;
         }
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int i = 0; i < C::HALF; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], s[i]);
+        float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
         const float m_tile = mx * c;  // finite: every tile has at least one valid key
         const bool grow = m_tile > m_run + 8.0f;
         const float m_new = grow ? m_tile : m_run;
-        const float alpha = grow ? exp2f(m_run - m_new) : 1.0f;  // exp2(-inf) = 0 on the first tile
-        float rs = 0.0f;
+        const float alpha = grow ? ex2_approx(m_run - m_new) : 1.0f;  // exp2(-inf) = 0 on the first tile
+        // p = 2^(s*c - m): one FFMA and one MUFU ex2 per score; masked keys of a partially filled
+        // tile get p = 0 explicitly (a zero scale would turn -inf * 0 into NaN)
+        float rs4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         uint32_t pk[C::HALF / 2];
+        if (n_valid < C::BN) {
 #pragma unroll
-        for (int i = 0; i < C::HALF; i += 2) {
-          const float p0 = (kbase + i < n_valid) ? exp2f(fmaf(s[i], c, -m_new)) : 0.0f;
-          const float p1 = (kbase + i + 1 < n_valid) ? exp2f(fmaf(s[i + 1], c, -m_new)) : 0.0f;
-          rs += p0 + p1;
-          pk[i / 2] = f32x2_to_bf16x2(p0, p1);
+          for (int i = 0; i < C::HALF; i += 2) {
+            const float p0 = kbase + i < n_valid ? ex2_approx(fmaf(s[i], c, -m_new)) : 0.0f;
+            const float p1 = kbase + i + 1 < n_valid ? ex2_approx(fmaf(s[i + 1], c, -m_new)) : 0.0f;
+            rs4[(i >> 1) & 3] += p0 + p1;
+            pk[i / 2] = f32x2_to_bf16x2(p0, p1);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < C::HALF; i += 2) {
+            const float p0 = ex2_approx(fmaf(s[i], c, -m_new));
+            const float p1 = ex2_approx(fmaf(s[i + 1], c, -m_new));
+            rs4[(i >> 1) & 3] += p0 + p1;
+            pk[i / 2] = f32x2_to_bf16x2(p0, p1);
+          }
         }
+        const float rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
         l_part = l_part * alpha + rs;
         // P buffer reuse and O rescale need the previous PV to be complete
         if (g > 0 && !wait(pv_done, (g - 1) & 1)) break;
         tc_fence_after();
-        if (grow && !first) {
+        // tcgen05.ld/st are warp-collective: the warp rescales if any of its heads grew, each
+        // thread with its own factor (1 for heads that did not grow)
+        if (__any_sync(0xffffffffu, grow && !first)) {
           const uint32_t oa = trow + C::O_COL;
           uint32_t r[32];
 #pragma unroll 1
@@ -561,9 +633,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           bool ok = true;
           for (int k = 1; k <= nparts && ok; ++k) {
             int v = 0;
-            for (uint32_t it = 0; it < (1u << 22); ++it) {
+            const uint64_t t0 = globaltimer_ns();
+            for (;;) {
               asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p.flags + 4 * (b + k) + sp) : "memory");
-              if (v) break;
+              if (v || globaltimer_ns() - t0 > 2000000000ull) break;
               __nanosleep(64);
             }
             if (!v) ok = false;
@@ -589,7 +662,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll 1
           for (int c0 = 0; c0 < C::DVC / 2; c0 += 32) {
             float acc[32];
-            if (w_own > 0.0f) {
+            if (had) {  // warp-uniform: every thread of the warp saw the same meta entry
               tmem_ld16x2_x32<128>(oa + c0, r);
               tc_wait_ld();
 #pragma unroll
@@ -634,26 +707,58 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       ++mc;
     }
   } else if (warp >= 8) {
-    // ==================================================== FP8 dequant (8 warps) ====
-    if constexpr (C::KIND == DSA_CACHE_FP8_SCALED) {
-      const int dw = warp - 8;
-      constexpr int RPW = C::BN / C::NDEQ;  // rows per warp per tile
-      constexpr int PARTS = C::D_NOPE / 256;
-      uint32_t mc = 0, g = 0;
-      while (!*abort_flag) {
-        const int st = mc % C::MSTAGES;
-        if (!wait(m_full(st), (mc / C::MSTAGES) & 1)) break;
-        const MetaHdr* mh = reinterpret_cast<const MetaHdr*>(smem + C::META_OFF + st * C::META_BYTES);
-        const int type = mh->type;
-        if (type != kTile) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(m_empty(st));
-          ++mc;
-          if (type == kDone) break;
-          continue;
+    // ====================================================== row loaders (8 warps) ====
+    // Warp dw fills rows dw, dw + 8, ... of each K tile in the 128-byte-swizzled K-major layout
+    // (row r, 16-byte granule g of 64-element chunk c at c*BN*128 + r*128 + ((g ^ (r&7)) << 4)).
+    // bf16 rows: cp.async 16-byte copies (rows past n_valid zero-filled), completion counted
+    // on the stage barrier per thread. Packed FP8 rows: codes and tile scales are loaded
+    // (already pulled into L2 by the producer), widened to bf16(code * scale) and stored.
+    const int dw = warp - 8;
+    constexpr int RPW = C::BN / C::NDEQ;  // rows per warp per tile
+    uint32_t mc = 0, g = 0;
+    while (!*abort_flag) {
+      const int st = mc % C::MSTAGES;
+      if (!wait(m_full(st), (mc / C::MSTAGES) & 1)) break;
+      const MetaHdr* mh = reinterpret_cast<const MetaHdr*>(smem + C::META_OFF + st * C::META_BYTES);
+      const int type = mh->type;
+      if (type != kTile) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(m_empty(st));
+        ++mc;
+        if (type == kDone) break;
+        continue;
+      }
+      const int n_valid = mh->n_valid;
+      const int* slots = reinterpret_cast<const int*>(reinterpret_cast<const uint8_t*>(mh) + 32);
+      const int ks = g % C::KSTAGES;
+      uint8_t* kt = smem + C::KT_OFF + ks * C::KT_BYTES;
+      if constexpr (C::KIND == DSA_CACHE_BF16) {
+        if (g >= (uint32_t)C::KSTAGES && !wait(k_empty(ks), ((g / C::KSTAGES) & 1) ^ 1)) break;
+        constexpr int GR = C::DK / 8;  // 16-byte granules per row
+#pragma unroll 2
+        for (int k = 0; k < RPW; ++k) {
+          const int r = dw + C::NDEQ * k;
+          const bool v = r < n_valid;
+          const uint8_t* row = p.cache + (v ? (int64_t)slots[r] : 0) * (2 * C::DK);
+#pragma unroll
+          for (int q0 = 0; q0 < GR; q0 += 32) {
+            const int q = q0 + lane;
+            if (q < GR) {
+              const int ch = q >> 3, gr = q & 7;
+              const uint32_t dst = smem_u32(kt + ch * (C::BN * 128) + r * 128 + ((gr ^ (r & 7)) << 4));
+              asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(row + 16 * q),
+                           "r"(v ? 16 : 0)
+                           : "memory");
+            }
+          }
         }
-        const int n_valid = mh->n_valid;
-        const int* slots = reinterpret_cast<const int*>(reinterpret_cast<const uint8_t*>(mh) + 32);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(m_empty(st));
+        ++mc;
+        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(k_full(ks)) : "memory");
+        ++g;
+      } else {
+        constexpr int PARTS = C::D_NOPE / 256;
         uint2 codes[RPW][PARTS];
         float scl[RPW][PARTS];
         uint4 rope[RPW];
@@ -677,9 +782,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(m_empty(st));
         ++mc;
-        const int ks = g % C::KSTAGES;
         if (g >= (uint32_t)C::KSTAGES && !wait(k_empty(ks), ((g / C::KSTAGES) & 1) ^ 1)) break;
-        uint8_t* kt = smem + C::KT_OFF + ks * C::KT_BYTES;
 #pragma unroll
         for (int k = 0; k < RPW; ++k) {
           const int r = dw + C::NDEQ * k;
@@ -718,6 +821,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         ++g;
       }
     }
+    // drain this thread's outstanding cp.async copies before the CTA can finish
+    asm volatile("cp.async.wait_all;" ::: "memory");
   }
 
   tc_fence_before();
@@ -772,7 +877,7 @@ static dsa_status_t launch(const dsa_attn_args_t* a, const DeviceInfo& dev, cuda
   dsa_status_t st = get_encode_fn(&encode);
   if (st != DSA_OK) return st;
 
-  CUtensorMap tq, tkv;
+  CUtensorMap tq;
   {
     const cuuint64_t dims[3] = {(cuuint64_t)C::DK, (cuuint64_t)kHeads, (cuuint64_t)a->T};
     const cuuint64_t strides[2] = {(cuuint64_t)a->q_stride_h * 2, (cuuint64_t)a->q_stride_t * 2};
@@ -782,18 +887,6 @@ static dsa_status_t launch(const dsa_attn_args_t* a, const DeviceInfo& dev, cuda
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
-  }
-  if (C::KIND == DSA_CACHE_BF16) {
-    const cuuint64_t dims[2] = {(cuuint64_t)C::DK, (cuuint64_t)a->num_slots};
-    const cuuint64_t strides[1] = {(cuuint64_t)C::DK * 2};
-    const cuuint32_t box[2] = {64, 1};
-    const cuuint32_t es[2] = {1, 1};
-    CUresult r = encode(&tkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a->cache), dims, strides, box, es,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
-  } else {
-    tkv = tq;  // unused by the FP8 kernels
   }
 
   AttnParams p{};
@@ -820,7 +913,10 @@ static dsa_status_t launch(const dsa_attn_args_t* a, const DeviceInfo& dev, cuda
   p.T = a->T;
   p.NT = (a->topk + C::BN - 1) / C::BN;
   p.U = a->T * C::DV_SPLIT * (int64_t)p.NT;
-  p.G = (int)(p.U < dev.sm_count ? p.U : dev.sm_count);
+  // one persistent CTA per SM, but at least 4 units per CTA so that small batches split each
+  // token into few parts (fewer partials to merge)
+  const int64_t g_cap = (p.U + 3) / 4;
+  p.G = (int)(g_cap < dev.sm_count ? g_cap : dev.sm_count);
 
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)p.G);
@@ -832,7 +928,7 @@ static dsa_status_t launch(const dsa_attn_args_t* a, const DeviceInfo& dev, cuda
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, dsa_attn_kernel<C>, p, tq, tkv);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, dsa_attn_kernel<C>, p, tq);
   return e == cudaSuccess ? DSA_OK : cuda_fail(e);
 }
 

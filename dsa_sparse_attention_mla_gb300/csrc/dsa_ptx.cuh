@@ -36,13 +36,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait: spins until the phase with the given parity has completed, or gives up after
-// `limit` polls (each poll may itself suspend for a hardware-chosen interval). Returns false on
-// timeout; the caller records DSA_DEVERR_TIMEOUT and drains.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit = (1u << 24)) {
-  for (uint32_t i = 0; i < limit; ++i)
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait: polls until the phase with the given parity has completed, or gives up once
+// `limit_ns` of wall time (the GPU's global timer) has passed. Returns false on timeout; the
+// caller records DSA_DEVERR_TIMEOUT and stops issuing work.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = 2000000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-  return false;
+    if ((i & 63) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+  }
 }
 
 // ------------------------------------------------------------------------- async copies --
@@ -178,6 +187,13 @@ __device__ __forceinline__ void tmem_st16x2_x32(uint32_t taddr, const uint32_t (
       "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
       "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
+}
+
+// 2^x on the MUFU unit (flushes subnormal results to zero; exp2(-inf) = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
 }
 
 // ------------------------------------------------------------------------ FP8 helpers --
