@@ -9,8 +9,9 @@
  *   - Contract table, "scaled FP8 cache row": 264 bytes = 256 e4m3 + 2 fp32 scales + 0 RoPE,
  *     656 bytes = 512 e4m3 + 4 fp32 scales + 64 bf16 RoPE values;
  *   - Scope list: quant_k_cache (pack rows), dequant_k_cache (direct, paged, gather/dequant);
- *   - Direct GLM geometry coverage list: top-k widths 2048 / 2112, rows padded with -1,
- *     "gather/mask/score/softmax/value", bit-identical repeated execution.
+ *   - Direct GLM geometry coverage list: top-k widths 2048 / 2112, rows padded with -1, the
+ *     reference computation (gather the rows, mask padding, score, softmax, weight the rows),
+ *     and repeated runs that agree bit for bit.
  *
  * Conventions for every entry point:
  *   - All pointers are DEVICE pointers unless stated otherwise; the caller owns all memory.
@@ -157,6 +158,7 @@ DSA_API dsa_status_t dsa_sparse_attn_workspace_size(const dsa_attn_args_t* args,
  * the same inputs on the same device.
  */
 DSA_API dsa_status_t dsa_sparse_attn(const dsa_attn_args_t* args, void* stream);
+
 
 #ifdef __cplusplus
 }

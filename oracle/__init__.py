@@ -11,7 +11,7 @@ bytes handed to the GPU are the bytes the oracle reads.
 
 Sources (sglang PR #38547 "Enable zero-RoPE TileLang DSA on gfx950"): the Contract table (packed
 row of 264 / 656 bytes; paged dequant/gather), the Scope list (quant_k_cache, dequant_k_cache)
-and the Direct GLM geometry coverage list (explicit gather/mask/score/softmax/value oracle).
+and the Direct GLM geometry coverage list (the step-by-step reference attention its tests use).
 """
 from __future__ import annotations
 

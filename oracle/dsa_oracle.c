@@ -11,11 +11,11 @@
  *     = 264 bytes for 256+0, 656 bytes for 512+64;
  *   - quant_k_cache / dequant_k_cache (Scope list) and the paged gather of rows
  *     (Contract table, "paged dequant/gather");
- *   - the sparse attention the pages check against "an explicit Torch gather/mask/score/
- *     softmax/value oracle" (Direct GLM geometry coverage list): per query token, gather the
- *     top-k latent rows named by its index list, mask entries < 0, score every head against
- *     every gathered row, softmax, and take the weighted sum of the same latent rows (the first
- *     d_v elements) as values.
+ *   - the sparse attention that the pages' tests use as their reference, written out step by
+ *     step (Direct GLM geometry coverage list): per query token, gather the top-k latent rows
+ *     named by its index list, mask entries < 0, score every head against every gathered row,
+ *     softmax, and take the weighted sum of the same latent rows (the first d_v elements) as
+ *     values.
  *
  * Readings where the pages are silent (each is also listed in the design notes):
  *   - scale = amax / 448 in fp32 (one IEEE division); codes = e4m3_rne_satfinite(x / scale),

@@ -1,5 +1,5 @@
-"""GPU parity of dsa_sparse_attn against the fp64 oracle (explicit gather/mask/score/softmax/
-value), over the geometry coverage of sglang PR #38547 (Direct GLM geometry coverage list):
+"""GPU parity of dsa_sparse_attn against the fp64 oracle (step-by-step gather, mask, score,
+softmax and weighted sum), over the geometry coverage of sglang PR #38547 (Direct GLM geometry coverage list):
 Q [tokens, 64, 256] with token counts 1, 8, 17; top-k widths 2048 and 2112; fully valid rows and
 2051 valid entries padded with -1 to 2112; BF16 and packed-FP8 caches; direct and paged slots;
 the 512+64 control; bit-identical repeated execution; and edge cases (masked tokens, a single

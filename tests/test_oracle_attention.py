@@ -1,4 +1,4 @@
-"""Pins of the oracle's sparse attention (explicit gather/mask/score/softmax/value) against
+"""Pins of the oracle's sparse attention (step-by-step gather, mask, score, softmax, weighted sum) against
 dense attention from a library routine, closed forms and invariances.
 
 The attention the pages check (sglang PR #38547, Direct GLM geometry coverage list): per token
