@@ -22,7 +22,7 @@ __all__ = [
     "DsaError", "CACHE_BF16", "CACHE_FP8_SCALED", "DEVERR_INDEX_OUT_OF_RANGE", "DEVERR_TIMEOUT",
     "DEVERR_SLOT_OUT_OF_RANGE", "library_path", "load_library", "dsa_status_string",
     "dsa_packed_row_bytes", "dsa_cache_row_bytes", "dsa_quant_k_cache", "dsa_gather_dequant",
-    "dsa_sparse_attn_workspace_size", "dsa_sparse_attn", "DsaAttnArgs",
+    "dsa_sparse_attn_workspace_size", "dsa_sparse_attn", "dsa_sparse_attn_static_ws", "DsaAttnArgs",
 ]
 
 CACHE_BF16 = 0
@@ -91,6 +91,8 @@ def load_library():
         lib.dsa_sparse_attn_workspace_size.restype = i32
         lib.dsa_sparse_attn.argtypes = [ctypes.POINTER(DsaAttnArgs), P]
         lib.dsa_sparse_attn.restype = i32
+        lib.dsa_sparse_attn_static_ws.argtypes = [ctypes.POINTER(DsaAttnArgs), P]
+        lib.dsa_sparse_attn_static_ws.restype = i32
         _LIB = lib
         return lib
 
@@ -274,4 +276,25 @@ def dsa_sparse_attn(q, cache, kind: int, indices, sm_scale: float, *, d_nope: in
     a = _attn_args(q, cache, kind, indices, sm_scale, d_nope, d_rope, d_v, block_table, page_size, req_of_token,
                    out, lse, workspace, error_word)
     _check(load_library().dsa_sparse_attn(ctypes.byref(a), _stream(q.device)), "dsa_sparse_attn")
+    return out
+
+
+def dsa_sparse_attn_static_ws(q, cache, kind: int, indices, sm_scale: float, *, d_nope: int = 256, d_rope: int = 0,
+                              d_v: int = None, block_table=None, page_size: int = 0, req_of_token=None, out=None,
+                              lse=None, error_word=None):
+    """dsa_sparse_attn without a workspace: the library's built-in device scratch is used, so
+    nothing is allocated by the call (for callers that cannot allocate, e.g. while a CUDA graph
+    is being captured). The first call on a device must come before any stream capture."""
+    import torch
+
+    d_v = d_nope if d_v is None else d_v
+    _need_cuda("q", q, torch.bfloat16)
+    _need_cuda("indices", indices, torch.int32)
+    if kind == CACHE_BF16 and cache.dim() == 3:
+        cache = cache.view(cache.shape[0], -1)
+    if out is None:
+        out = torch.empty((q.shape[0], q.shape[1], d_v), dtype=torch.bfloat16, device=q.device)
+    a = _attn_args(q, cache, kind, indices, sm_scale, d_nope, d_rope, d_v, block_table, page_size, req_of_token,
+                   out, lse, None, error_word)
+    _check(load_library().dsa_sparse_attn_static_ws(ctypes.byref(a), _stream(q.device)), "dsa_sparse_attn_static_ws")
     return out

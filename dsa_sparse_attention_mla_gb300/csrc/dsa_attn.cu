@@ -998,3 +998,69 @@ dsa_status_t dsa_sparse_attn(const dsa_attn_args_t* a, void* stream) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------- fixed-scratch entry point --
+// Some callers cannot allocate device memory at call time: code running while a CUDA graph
+// is being captured on a stream (where cudaMalloc is not allowed), allocator-free runtimes and
+// embedded hosts that only hand the library input and output buffers. For them,
+// dsa_sparse_attn_static_ws takes its scratch (split-token partials and their flags) from
+// this file-scope device array instead of a caller-supplied workspace. It holds the partials
+// of at most kStaticWsCtas CTAs (about 10.6 MB); every GPU that loads the library keeps it
+// until the process exits.
+namespace dsa {
+constexpr int kStaticWsCtas = 160;
+constexpr size_t kStaticWsBytes = (size_t)kStaticWsCtas * kHeads * 256 * 4 + (size_t)kStaticWsCtas * 2 * kHeads * 4 +
+                                  (((size_t)kStaticWsCtas * 16 + 255) & ~size_t(255));
+static __device__ __align__(256) uint8_t g_static_ws[kStaticWsBytes];
+
+// Device address of g_static_ws for the current device, looked up once per device (the host
+// name of the array is only a stand-in and must never be passed to a kernel).
+static dsa_status_t static_ws_ptr(int device, void** out) {
+  static std::mutex mu;
+  static void* ptrs[64] = {};
+  if (device < 0 || device >= 64) return DSA_ERR_NO_DEVICE;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[device]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_static_ws);
+    if (e != cudaSuccess) return cuda_fail(e);
+    ptrs[device] = p;
+  }
+  *out = ptrs[device];
+  return DSA_OK;
+}
+}  // namespace dsa
+
+extern "C" dsa_status_t dsa_sparse_attn_static_ws(const dsa_attn_args_t* a, void* stream) {
+  if (!a) return DSA_ERR_INVALID_ARGUMENT;
+  // the caller's workspace fields are ignored; the other arguments follow dsa_sparse_attn's
+  // rules (the placeholder only satisfies the workspace check and is never dereferenced)
+  dsa_attn_args_t b = *a;
+  b.workspace = reinterpret_cast<void*>(uintptr_t(256));
+  b.workspace_bytes = 0;
+  dsa_status_t st = validate(&b);
+  if (st != DSA_OK || b.T == 0) return st;
+  DeviceInfo dev;
+  st = current_device(&dev);
+  if (st != DSA_OK) return st;
+  // at most kStaticWsCtas persistent CTAs: their partials must fit in the fixed array
+  DeviceInfo capped = dev;
+  if (capped.sm_count > kStaticWsCtas) capped.sm_count = kStaticWsCtas;
+  if (ws_bytes_for(capped.sm_count) > kStaticWsBytes) return DSA_ERR_WORKSPACE_TOO_SMALL;
+  void* ws = nullptr;
+  st = static_ws_ptr(dev.device, &ws);
+  if (st != DSA_OK) return st;
+  b.workspace = ws;
+  b.workspace_bytes = kStaticWsBytes;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the flags must start at zero: a call that stopped on a timeout may have left some set
+  const size_t flags_off = (size_t)capped.sm_count * kHeads * 256 * 4 + (size_t)capped.sm_count * 2 * kHeads * 4;
+  cudaError_t e = cudaMemsetAsync(static_cast<uint8_t*>(ws) + flags_off, 0, (size_t)capped.sm_count * 16, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (b.d_nope == 256) {
+    if (b.kind == DSA_CACHE_BF16) return launch<CfgBf16_256>(&b, capped, s);
+    return launch<CfgFp8_256>(&b, capped, s);
+  }
+  if (b.kind == DSA_CACHE_BF16) return launch<CfgBf16_576>(&b, capped, s);
+  return launch<CfgFp8_576>(&b, capped, s);
+}

@@ -159,6 +159,29 @@ DSA_API dsa_status_t dsa_sparse_attn_workspace_size(const dsa_attn_args_t* args,
  */
 DSA_API dsa_status_t dsa_sparse_attn(const dsa_attn_args_t* args, void* stream);
 
+/*
+ * dsa_sparse_attn_static_ws - dsa_sparse_attn for callers that cannot allocate device memory.
+ * (No counterpart on the pages: this is a deployment variant of the same computation.)
+ *
+ * Who needs it: code that enqueues work while a CUDA graph is being captured (cudaMalloc is
+ * not allowed then), allocator-free runtimes, and hosts that hand the library only its input
+ * and output buffers. Instead of args->workspace (ignored, together with workspace_bytes),
+ * the split-token scratch lives in a fixed device array inside the library: about 10.6 MB,
+ * enough for the partial results of up to 160 CTAs. Every GPU that loads the library holds
+ * that array until the process exits. The call allocates nothing.
+ *
+ * Arguments, results and errors are those of dsa_sparse_attn; the result is identical to
+ * dsa_sparse_attn's on GPUs with at most 160 SMs. On a GPU with more SMs the kernel runs on 160
+ * CTAs; if the array could not hold the scratch of the launch the call returns
+ * DSA_ERR_WORKSPACE_TOO_SMALL without launching.
+ *
+ * The first call on each device looks up the array's device address (set-up that is not
+ * allowed inside a stream capture): make that first call, per device, before capturing.
+ * All calls share the one array and each clears the flags it relies on before launching, so
+ * two calls whose kernels overlap on the GPU (different streams, no ordering between them)
+ * race on it: order such calls, or use dsa_sparse_attn with separate workspaces.
+ */
+DSA_API dsa_status_t dsa_sparse_attn_static_ws(const dsa_attn_args_t* args, void* stream);
 
 #ifdef __cplusplus
 }
