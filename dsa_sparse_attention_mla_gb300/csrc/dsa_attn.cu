@@ -27,6 +27,7 @@
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <unordered_map>
 
 #include "dsa_host.h"
 #include "dsa_ptx.cuh"
@@ -109,7 +110,8 @@ struct AttnParams {
   float* lse;
   float* ws_o;    // [G][64][256] partial o (unnormalised, relative to its max)
   float* ws_ml;   // [G][2][64] partial max (log2 domain) and sum
-  int* flags;     // [G][4] partial published, one flag per softmax warp (16 heads)
+  int* flags;     // [G][4] partial published (holds the call's epoch), one per softmax warp
+  int epoch;      // this call's tag for the flags (never 0); stale flags from older calls differ
   int32_t* err;
   int64_t T;
   int NT;         // key tiles per token (over the index width)
@@ -368,7 +370,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       constexpr uint32_t idS = idesc_bf16(64, C::BN, 0, 0);
       constexpr uint32_t idPV = idesc_bf16(64, C::DVC, 0, 1);
       uint32_t mc = 0, g = 0, qc = 0;
-      int pend = -1, pend_first = 0, pend_dvh = 0;
       // Descriptors are built once; the k-step offsets are compile-time adds on the 16-byte
       // address field (every operand stays below 256 KB of shared memory).
       const uint64_t dQ = sw128_desc(sbase + C::Q_OFF, 16, 1024);
@@ -388,57 +389,89 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         mma_commit(k_empty(ks));
         mma_commit(pv_done);
       };
-      while (!*abort_flag) {
-        const int st = mc % C::MSTAGES;
-        if (!wait(m_full(st), (mc / C::MSTAGES) & 1)) break;
-        const MetaHdr* mh = reinterpret_cast<const MetaHdr*>(smem + C::META_OFF + st * C::META_BYTES);
-        const int type = mh->type;
-        if (type == kTile) {
-          const int first = mh->first;
-          const int dvh = mh->vtoken % C::DV_SPLIT;
-          mbar_arrive(m_empty(st));
-          if (first) {
-            if (!wait(q_full, qc & 1)) break;
-            ++qc;
-          }
-          const int ks = g % C::KSTAGES;
-          if (!wait(k_full(ks), (g / C::KSTAGES) & 1)) break;
-          if (g >= 2 && !wait(s_empty(g & 1), ((g >> 1) & 1) ^ 1)) break;
-          // bf16 rows arrive by cp.async, i.e. through the generic proxy: order them before the
-          // tensor core reads (the FP8 loaders fence on their side before arriving)
-          if constexpr (C::KIND == DSA_CACHE_BF16) fence_proxy_async_smem();
-          tc_fence_after();
-          const uint64_t dK = sw128_desc(sbase + C::KT_OFF + ks * C::KT_BYTES, 16, 1024);
+      // Event-driven issue: poll (without blocking) for the oldest tile whose P is ready and for
+      // the next tile whose K stage, S buffer (and Q) are ready; issue whichever is ready,
+      // PV first since it frees a K stage. Meta entries are consumed as S advances (segment
+      // ends release the Q buffer once the segment's S products are issued).
+      uint32_t gP = 0;             // PV products issued (gP <= g, the S products issued)
+      int t_first[4] = {0, 0, 0, 0}, t_dvh[4] = {0, 0, 0, 0};
+      bool done = false, have = false, q_ok = false;
+      int cur_first = 0, cur_dvh = 0;
+      uint64_t last_progress = globaltimer_ns();
+      auto try_pv = [&](uint32_t limit) -> bool {  // issue PV(gP) if its P is ready
+        if (gP < limit && mbar_test(p_full, gP & 1)) {
+          issue_pv(gP, t_first[gP & 3], t_dvh[gP & 3]);
+          ++gP;
+          return true;
+        }
+        return false;
+      };
+      auto issue_s = [&](uint32_t gg) {
+        const int ks = gg % C::KSTAGES;
+        // bf16 rows arrive by cp.async, i.e. through the generic proxy: order them before the
+        // tensor core reads (the FP8 loaders fence on their side before arriving)
+        if constexpr (C::KIND == DSA_CACHE_BF16) fence_proxy_async_smem();
+        tc_fence_after();
+        const uint64_t dK = sw128_desc(sbase + C::KT_OFF + ks * C::KT_BYTES, 16, 1024);
+        // four k-steps at a time, so that a PV whose P became ready is not queued behind the
+        // whole S product
 #pragma unroll
-          for (int kk = 0; kk < C::DK / 16; ++kk) {
-            const uint64_t qa = (uint64_t)(((kk >> 2) * (kHeads * 128) + (kk & 3) * 32) >> 4);
-            const uint64_t ka = (uint64_t)(((kk >> 2) * (C::BN * 128) + (kk & 3) * 32) >> 4);
-            mma_bf16(tmem + C::S_COL + (g & 1) * C::BN, dQ + qa, dK + ka, idS, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < C::DK / 16; ++kk) {
+          const uint64_t qa = (uint64_t)(((kk >> 2) * (kHeads * 128) + (kk & 3) * 32) >> 4);
+          const uint64_t ka = (uint64_t)(((kk >> 2) * (C::BN * 128) + (kk & 3) * 32) >> 4);
+          mma_bf16(tmem + C::S_COL + (gg & 1) * C::BN, dQ + qa, dK + ka, idS, kk > 0 ? 1u : 0u);
+          if ((kk & 3) == 3 && kk + 1 < C::DK / 16) try_pv(gg);
+        }
+        mma_commit(s_full(gg & 1));
+      };
+      while (!*abort_flag && (!done || gP < g)) {
+        bool progress = false;
+        if (try_pv(g)) {
+          progress = true;
+        } else if (!done) {
+          if (!have) {
+            const int st = mc % C::MSTAGES;
+            if (mbar_test(m_full(st), (mc / C::MSTAGES) & 1)) {
+              const MetaHdr* mh = reinterpret_cast<const MetaHdr*>(smem + C::META_OFF + st * C::META_BYTES);
+              const int type = mh->type;
+              if (type == kTile) {
+                cur_first = mh->first;
+                cur_dvh = mh->vtoken % C::DV_SPLIT;
+                have = true;
+              } else if (type == kSegEnd) {
+                if (mh->had_tiles) mma_commit(q_empty);
+              } else {
+                done = true;
+              }
+              mbar_arrive(m_empty(st));
+              ++mc;
+              progress = true;
+            }
           }
-          mma_commit(s_full(g & 1));
-          if (pend >= 0) issue_pv((uint32_t)pend, pend_first, pend_dvh);
-          pend = (int)g;
-          pend_first = first;
-          pend_dvh = dvh;
-          ++g;
-        } else if (type == kSegEnd) {
-          const int had = mh->had_tiles;
-          mbar_arrive(m_empty(st));
-          if (had) mma_commit(q_empty);
-          // finish the segment's last PV now rather than after the next segment's first S, so
-          // the epilogue does not wait for the next Q load
-          if (pend >= 0) {
-            issue_pv((uint32_t)pend, pend_first, pend_dvh);
-            pend = -1;
+          if (have) {
+            if (cur_first && !q_ok && mbar_test(q_full, qc & 1)) {
+              q_ok = true;
+              ++qc;
+            }
+            if ((!cur_first || q_ok) && mbar_test(k_full(g % C::KSTAGES), (g / C::KSTAGES) & 1) &&
+                (g < 2 || mbar_test(s_empty(g & 1), ((g >> 1) & 1) ^ 1))) {
+              issue_s(g);
+              t_first[g & 3] = cur_first;
+              t_dvh[g & 3] = cur_dvh;
+              ++g;
+              have = false;
+              q_ok = false;
+              progress = true;
+            }
           }
-        } else {
-          mbar_arrive(m_empty(st));
-          ++mc;
+        }
+        if (progress) {
+          last_progress = globaltimer_ns();
+        } else if (globaltimer_ns() - last_progress > 2000000000ull) {
+          fail(DSA_DEVERR_TIMEOUT);
           break;
         }
-        ++mc;
       }
-      if (pend >= 0 && !*abort_flag) issue_pv((uint32_t)pend, pend_first, pend_dvh);
       // drain: wait for every MMA this thread issued before TMEM can be released
       if (g > 0) mbar_wait(pv_done, (g - 1) & 1);
     }
@@ -626,7 +659,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           __threadfence();
           __syncwarp();
           if (lane == 0)
-            asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.flags + 4 * b + sp), "r"(1) : "memory");
+            asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.flags + 4 * b + sp), "r"(p.epoch) : "memory");
         } else {
           // complete token, or the head of a split token: merge parts b+1..last in order
           const int nparts = kind == kHead ? last - b : 0;
@@ -636,10 +669,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const uint64_t t0 = globaltimer_ns();
             for (;;) {
               asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p.flags + 4 * (b + k) + sp) : "memory");
-              if (v || globaltimer_ns() - t0 > 2000000000ull) break;
+              if (v == p.epoch || globaltimer_ns() - t0 > 2000000000ull) break;
               __nanosleep(64);
             }
-            if (!v) ok = false;
+            if (v != p.epoch) ok = false;
           }
           if (!ok) fail(DSA_DEVERR_TIMEOUT);
           float M = m_row;
@@ -696,11 +729,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           }
           if (p.lse && dvh == 0 && hf == 0)
             p.lse[t * kHeads + h] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
-          if (nparts > 0) {
-            __syncwarp();
-            if (lane == 0)
-              for (int k = 1; k <= nparts; ++k) p.flags[4 * (b + k) + sp] = 0;
-          }
+
         }
         tc_fence_before();
       }
@@ -716,23 +745,23 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const int dw = warp - 8;
     constexpr int RPW = C::BN / C::NDEQ;  // rows per warp per tile
     uint32_t mc = 0, g = 0;
-    while (!*abort_flag) {
-      const int st = mc % C::MSTAGES;
-      if (!wait(m_full(st), (mc / C::MSTAGES) & 1)) break;
-      const MetaHdr* mh = reinterpret_cast<const MetaHdr*>(smem + C::META_OFF + st * C::META_BYTES);
-      const int type = mh->type;
-      if (type != kTile) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(m_empty(st));
-        ++mc;
-        if (type == kDone) break;
-        continue;
-      }
-      const int n_valid = mh->n_valid;
-      const int* slots = reinterpret_cast<const int*>(reinterpret_cast<const uint8_t*>(mh) + 32);
-      const int ks = g % C::KSTAGES;
-      uint8_t* kt = smem + C::KT_OFF + ks * C::KT_BYTES;
-      if constexpr (C::KIND == DSA_CACHE_BF16) {
+    if constexpr (C::KIND == DSA_CACHE_BF16) {
+      while (!*abort_flag) {
+        const int st = mc % C::MSTAGES;
+        if (!wait(m_full(st), (mc / C::MSTAGES) & 1)) break;
+        const MetaHdr* mh = reinterpret_cast<const MetaHdr*>(smem + C::META_OFF + st * C::META_BYTES);
+        const int type = mh->type;
+        if (type != kTile) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(m_empty(st));
+          ++mc;
+          if (type == kDone) break;
+          continue;
+        }
+        const int n_valid = mh->n_valid;
+        const int* slots = reinterpret_cast<const int*>(reinterpret_cast<const uint8_t*>(mh) + 32);
+        const int ks = g % C::KSTAGES;
+        uint8_t* kt = smem + C::KT_OFF + ks * C::KT_BYTES;
         if (g >= (uint32_t)C::KSTAGES && !wait(k_empty(ks), ((g / C::KSTAGES) & 1) ^ 1)) break;
         constexpr int GR = C::DK / 8;  // 16-byte granules per row
 #pragma unroll 2
@@ -757,50 +786,80 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         ++mc;
         asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(k_full(ks)) : "memory");
         ++g;
-      } else {
-        constexpr int PARTS = C::D_NOPE / 256;
+      }
+    } else {
+      // Packed FP8 rows, two tiles in flight per warp (256+0): the loads of the next tile are
+      // issued before the current tile is converted (two register buffers, used alternately).
+      constexpr int PARTS = C::D_NOPE / 256;
+      struct Rows {
         uint2 codes[RPW][PARTS];
         float scl[RPW][PARTS];
         uint4 rope[RPW];
+        int n_valid;
+      };
+      // wait for the next tile's slot list (skipping segment ends), issue its row loads, and
+      // release the meta entry; false when the stream is done
+      // fetch() returns 1 when a tile was fetched, 0 at the end of the stream, and -1 (only
+      // when `block` is false) when the next entry is not published yet.
+      auto fetch = [&](Rows& R, bool block) -> int {
+        while (!*abort_flag) {
+          const int st = mc % C::MSTAGES;
+          if (!block && !mbar_test(m_full(st), (mc / C::MSTAGES) & 1)) return -1;
+          if (!wait(m_full(st), (mc / C::MSTAGES) & 1)) return 0;
+          const MetaHdr* mh = reinterpret_cast<const MetaHdr*>(smem + C::META_OFF + st * C::META_BYTES);
+          const int type = mh->type;
+          if (type == kTile) {
+            R.n_valid = mh->n_valid;
+            const int* slots = reinterpret_cast<const int*>(reinterpret_cast<const uint8_t*>(mh) + 32);
 #pragma unroll
-        for (int k = 0; k < RPW; ++k) {
-          const int r = dw + C::NDEQ * k;
-          if (r < n_valid) {
-            const uint8_t* row = p.cache + (int64_t)slots[r] * C::RB;
+            for (int k = 0; k < RPW; ++k) {
+              const int r = dw + C::NDEQ * k;
+              if (r < R.n_valid) {
+                const uint8_t* row = p.cache + (int64_t)slots[r] * C::RB;
 #pragma unroll
-            for (int pt = 0; pt < PARTS; ++pt) {
-              const int d0 = 256 * pt + 8 * lane;
-              codes[k][pt] = __ldg(reinterpret_cast<const uint2*>(row + d0));
-              scl[k][pt] = __ldg(reinterpret_cast<const float*>(row + C::D_NOPE + 4 * (d0 / 128)));
-            }
-            if constexpr (C::D_ROPE > 0) {
-              if (lane < C::D_ROPE / 8)
-                rope[k] = __ldg(reinterpret_cast<const uint4*>(row + C::D_NOPE + 4 * (C::D_NOPE / 128)) + lane);
+                for (int pt = 0; pt < PARTS; ++pt) {
+                  const int d0 = 256 * pt + 8 * lane;
+                  R.codes[k][pt] = __ldg(reinterpret_cast<const uint2*>(row + d0));
+                  R.scl[k][pt] = __ldg(reinterpret_cast<const float*>(row + C::D_NOPE + 4 * (d0 / 128)));
+                }
+                if constexpr (C::D_ROPE > 0) {
+                  if (lane < C::D_ROPE / 8)
+                    R.rope[k] = __ldg(reinterpret_cast<const uint4*>(row + C::D_NOPE + 4 * (C::D_NOPE / 128)) + lane);
+                }
+              }
             }
           }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(m_empty(st));
+          ++mc;
+          if (type == kTile) return 1;
+          if (type == kDone) return 0;
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(m_empty(st));
-        ++mc;
-        if (g >= (uint32_t)C::KSTAGES && !wait(k_empty(ks), ((g / C::KSTAGES) & 1) ^ 1)) break;
+        return 0;
+      };
+      // widen the rows of R into the next K stage and publish it
+      auto convert = [&](const Rows& R) -> bool {
+        const int ks = g % C::KSTAGES;
+        uint8_t* kt = smem + C::KT_OFF + ks * C::KT_BYTES;
+        if (g >= (uint32_t)C::KSTAGES && !wait(k_empty(ks), ((g / C::KSTAGES) & 1) ^ 1)) return false;
 #pragma unroll
         for (int k = 0; k < RPW; ++k) {
           const int r = dw + C::NDEQ * k;
-          const bool v = r < n_valid;
+          const bool v = r < R.n_valid;
 #pragma unroll
           for (int pt = 0; pt < PARTS; ++pt) {
             const int d0 = 256 * pt + 8 * lane;
             uint4 o = make_uint4(0, 0, 0, 0);
             if (v) {
-              const float sc = scl[k][pt];
-              const uint32_t cw[2] = {codes[k][pt].x, codes[k][pt].y};
+              const float sc = R.scl[k][pt];
+              const uint32_t cw[2] = {R.codes[k][pt].x, R.codes[k][pt].y};
               uint32_t w[4];
 #pragma unroll
               for (int q = 0; q < 2; ++q) {
-                const float2 a = f16x2_to_f32x2(e4m3x2_to_f16x2((uint16_t)(cw[q] & 0xFFFFu)));
-                const float2 bb = f16x2_to_f32x2(e4m3x2_to_f16x2((uint16_t)(cw[q] >> 16)));
-                w[2 * q] = f32x2_to_bf16x2(__fmul_rn(a.x, sc), __fmul_rn(a.y, sc));
-                w[2 * q + 1] = f32x2_to_bf16x2(__fmul_rn(bb.x, sc), __fmul_rn(bb.y, sc));
+                const float2 x0 = f16x2_to_f32x2(e4m3x2_to_f16x2((uint16_t)(cw[q] & 0xFFFFu)));
+                const float2 x1 = f16x2_to_f32x2(e4m3x2_to_f16x2((uint16_t)(cw[q] >> 16)));
+                w[2 * q] = f32x2_to_bf16x2(__fmul_rn(x0.x, sc), __fmul_rn(x0.y, sc));
+                w[2 * q + 1] = f32x2_to_bf16x2(__fmul_rn(x1.x, sc), __fmul_rn(x1.y, sc));
               }
               o = make_uint4(w[0], w[1], w[2], w[3]);
             }
@@ -811,7 +870,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             if (lane < C::D_ROPE / 8) {
               const int ch = C::D_NOPE / 64 + (lane >> 3), gr = lane & 7;
               *reinterpret_cast<uint4*>(kt + ch * (C::BN * 128) + r * 128 + ((gr ^ (r & 7)) << 4)) =
-                  v ? rope[k] : make_uint4(0, 0, 0, 0);
+                  v ? R.rope[k] : make_uint4(0, 0, 0, 0);
             }
           }
         }
@@ -819,6 +878,28 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(k_full(ks));
         ++g;
+        return true;
+      };
+      if constexpr (PARTS == 1) {
+        // The next tile is fetched ahead only when its entry is already published: waiting for
+        // it before converting the current tile could deadlock at a segment boundary (the next
+        // segment's first entry waits for its Q buffer, i.e. for this tile's S product).
+        Rows ra, rb;
+        int more = fetch(ra, true);
+        while (more == 1) {
+          int nb = fetch(rb, false);
+          if (!convert(ra)) break;
+          if (nb < 0) nb = fetch(rb, true);
+          if (nb == 0) break;
+          int na = fetch(ra, false);
+          if (!convert(rb)) break;
+          if (na < 0) na = fetch(ra, true);
+          more = na;
+        }
+      } else {  // 512+64 rows: one tile in flight (two would not fit in registers)
+        Rows ra;
+        while (fetch(ra, true) == 1 && convert(ra)) {
+        }
       }
     }
     // drain this thread's outstanding cp.async copies before the CTA can finish
@@ -863,6 +944,17 @@ static size_t ws_bytes_for(int sm_count) {
   const size_t ml = (size_t)sm_count * 2 * kHeads * 4;
   const size_t fl = ((size_t)sm_count * 16 + 255) & ~size_t(255);
   return o + ml + fl;
+}
+
+// Per-workspace call counter: the merge flags of a call carry its value, so flags left by an
+// earlier call (even one that stopped on a timeout) never match.
+static int next_epoch(const void* workspace) {
+  static std::mutex mu;
+  static std::unordered_map<const void*, int> epochs;
+  std::lock_guard<std::mutex> lock(mu);
+  int& e = epochs[workspace];
+  e = (e == 0x7FFFFFFF) ? 1 : e + 1;
+  return e;
 }
 
 template <class C>
@@ -910,6 +1002,7 @@ static dsa_status_t launch(const dsa_attn_args_t* a, const DeviceInfo& dev, cuda
   p.ws_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(a->workspace) + o_bytes);
   p.flags = reinterpret_cast<int*>(static_cast<uint8_t*>(a->workspace) + o_bytes + (size_t)dev.sm_count * 2 * kHeads * 4);
   p.err = a->error_word;
+  p.epoch = next_epoch(a->workspace);
   p.T = a->T;
   p.NT = (a->topk + C::BN - 1) / C::BN;
   p.U = a->T * C::DV_SPLIT * (int64_t)p.NT;
@@ -1053,10 +1146,8 @@ extern "C" dsa_status_t dsa_sparse_attn_static_ws(const dsa_attn_args_t* a, void
   b.workspace = ws;
   b.workspace_bytes = kStaticWsBytes;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the flags must start at zero: a call that stopped on a timeout may have left some set
-  const size_t flags_off = (size_t)capped.sm_count * kHeads * 256 * 4 + (size_t)capped.sm_count * 2 * kHeads * 4;
-  cudaError_t e = cudaMemsetAsync(static_cast<uint8_t*>(ws) + flags_off, 0, (size_t)capped.sm_count * 16, s);
-  if (e != cudaSuccess) return cuda_fail(e);
+  // nothing needs clearing: the array starts zero-filled and each call tags its merge flags
+  // with a fresh per-array epoch, so values left by an earlier call never match
   if (b.d_nope == 256) {
     if (b.kind == DSA_CACHE_BF16) return launch<CfgBf16_256>(&b, capped, s);
     return launch<CfgFp8_256>(&b, capped, s);

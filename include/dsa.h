@@ -135,8 +135,9 @@ typedef struct dsa_attn_args {
   int64_t out_stride_t, out_stride_h;
   float* lse;                    /* optional fp32 [T, H] natural-log sum of exp(scores); NULL ok */
   void* workspace;               /* device scratch of dsa_sparse_attn_workspace_size bytes,
-                                    zero-filled before its first use; every call leaves it
-                                    zero-filled again. One call at a time per workspace. */
+                                    zero-filled before its first use in a process (the library
+                                    tags its flags with a per-workspace call counter, so it never
+                                    needs clearing again). One call at a time per workspace. */
   size_t workspace_bytes;
   int32_t* error_word;           /* optional device int32; DSA_DEVERR_* bits are OR-ed in */
 } dsa_attn_args_t;
@@ -177,9 +178,10 @@ DSA_API dsa_status_t dsa_sparse_attn(const dsa_attn_args_t* args, void* stream);
  *
  * The first call on each device looks up the array's device address (set-up that is not
  * allowed inside a stream capture): make that first call, per device, before capturing.
- * All calls share the one array and each clears the flags it relies on before launching, so
- * two calls whose kernels overlap on the GPU (different streams, no ordering between them)
- * race on it: order such calls, or use dsa_sparse_attn with separate workspaces.
+ * All calls share the one array (its flags are tagged with a per-call epoch, so nothing has to
+ * be cleared between calls). Two calls whose kernels overlap on the GPU (different streams, no
+ * ordering between them) race on it: order such calls, or use dsa_sparse_attn with separate
+ * workspaces.
  */
 DSA_API dsa_status_t dsa_sparse_attn_static_ws(const dsa_attn_args_t* args, void* stream);
 
