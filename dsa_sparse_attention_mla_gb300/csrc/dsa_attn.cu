@@ -1,4 +1,7 @@
-// dsa_attn.cu - DSA sparse MLA attention forward for sm_103a (tcgen05 + TMEM + TMA).
+// dsa_attn.cu - DSA sparse MLA attention forward for sm_103a (tcgen05 + TMEM + TMA): the
+// entry points (argument checks, dispatch, workspace, fixed-scratch variant), the host pieces
+// shared with dsa_attn_k128.cu, and the kernel of the 512+64 control geometry. The 256+0
+// geometry runs in dsa_attn_k128.cu.
 //
 // What is computed (sglang PR #38547 "Enable zero-RoPE TileLang DSA on gfx950", Summary and
 // Direct GLM geometry coverage list): for every query token t and head h, gather the latent
@@ -6,11 +9,12 @@
 // softmax over j and return sum_j p_j * k_j[0:d_v] in bf16. The cache holds bf16 rows or the
 // packed scaled-FP8 rows of the Contract table (codes * per-128-tile fp32 scale).
 //
-// Kernel design (GB300-first, not the pages' TileLang/HIP kernels):
+// 512+64 kernel design:
 //  * Heads are the MMA M dimension (M = 64), gathered keys are N: S = Q K^T (K-dim = d) and
 //    O += P V (K-dim = keys, V = the first d_v columns of the same gathered rows) are dense
 //    tcgen05 kind::f16 contractions with fp32 accumulators in tensor memory. The M = 64
-//    accumulator occupies TMEM lanes 32*w + [0,16) of each sub-partition w.
+//    accumulator occupies TMEM lanes 32*w + [0,16) of each sub-partition w. d_v = 512 runs as
+//    two 256-column passes (TMEM holds O for 256 columns at a time).
 //  * One persistent CTA per SM, launched cooperatively. The (token, key-tile) units are split
 //    into equal contiguous ranges, one per CTA ("stream-K"); a token cut by a range boundary
 //    is finished by the CTA holding its first tiles, which merges the other CTAs' partial
@@ -21,7 +25,7 @@
 //    16-byte copies of bf16 rows, or loads of packed FP8 rows widened to bf16(code * scale),
 //    into the 128-byte-swizzled K-major tile.
 //  * Online softmax in the exp2 domain with a lazy rescale (O and the running sum are only
-//    rescaled when the running max grows by more than 2^8), zero-RoPE work compiled out.
+//    rescaled when the running max grows by more than 2^8).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -29,6 +33,7 @@
 #include <mutex>
 #include <unordered_map>
 
+#include "dsa_attn_common.h"
 #include "dsa_host.h"
 #include "dsa_ptx.cuh"
 
@@ -934,11 +939,21 @@ static dsa_status_t get_encode_fn(EncodeTiledFn* fn) {
   return DSA_OK;
 }
 
-struct Geometry {
-  int d_nope, d_rope, d_v, dv_split;
-};
+dsa_status_t encode_q_tensor_map(const dsa_attn_args_t* a, int dk, CUtensorMap* out) {
+  EncodeTiledFn encode;
+  dsa_status_t st = get_encode_fn(&encode);
+  if (st != DSA_OK) return st;
+  const cuuint64_t dims[3] = {(cuuint64_t)dk, (cuuint64_t)kHeads, (cuuint64_t)a->T};
+  const cuuint64_t strides[2] = {(cuuint64_t)a->q_stride_h * 2, (cuuint64_t)a->q_stride_t * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)kHeads, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a->q), dims, strides, box, es,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DSA_OK : cuda_fail(cudaErrorInvalidValue);
+}
 
-static size_t ws_bytes_for(int sm_count) {
+size_t attn_ws_bytes(int sm_count) {
   // partial o [G][64][256] fp32 + (max, sum) [G][2][64] fp32 + flags [G][4] int32
   const size_t o = (size_t)sm_count * kHeads * 256 * 4;
   const size_t ml = (size_t)sm_count * 2 * kHeads * 4;
@@ -946,9 +961,17 @@ static size_t ws_bytes_for(int sm_count) {
   return o + ml + fl;
 }
 
-// Per-workspace call counter: the merge flags of a call carry its value, so flags left by an
-// earlier call (even one that stopped on a timeout) never match.
-static int next_epoch(const void* workspace) {
+AttnWorkspace attn_ws_layout(void* workspace, int sm_count) {
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  const size_t o_bytes = (size_t)sm_count * kHeads * 256 * 4;
+  AttnWorkspace r;
+  r.o = reinterpret_cast<float*>(w);
+  r.ml = reinterpret_cast<float*>(w + o_bytes);
+  r.flags = reinterpret_cast<int*>(w + o_bytes + (size_t)sm_count * 2 * kHeads * 4);
+  return r;
+}
+
+int next_attn_epoch(const void* workspace) {
   static std::mutex mu;
   static std::unordered_map<const void*, int> epochs;
   std::lock_guard<std::mutex> lock(mu);
@@ -965,21 +988,9 @@ static dsa_status_t launch(const dsa_attn_args_t* a, const DeviceInfo& dev, cuda
     attr_err = cudaFuncSetAttribute(dsa_attn_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return cuda_fail(attr_err);
-  EncodeTiledFn encode;
-  dsa_status_t st = get_encode_fn(&encode);
-  if (st != DSA_OK) return st;
-
   CUtensorMap tq;
-  {
-    const cuuint64_t dims[3] = {(cuuint64_t)C::DK, (cuuint64_t)kHeads, (cuuint64_t)a->T};
-    const cuuint64_t strides[2] = {(cuuint64_t)a->q_stride_h * 2, (cuuint64_t)a->q_stride_t * 2};
-    const cuuint32_t box[3] = {64, (cuuint32_t)kHeads, 1};
-    const cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = encode(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a->q), dims, strides, box, es,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
-  }
+  dsa_status_t st = encode_q_tensor_map(a, C::DK, &tq);
+  if (st != DSA_OK) return st;
 
   AttnParams p{};
   p.cache = static_cast<const uint8_t*>(a->cache);
@@ -997,12 +1008,12 @@ static dsa_status_t launch(const dsa_attn_args_t* a, const DeviceInfo& dev, cuda
   p.out_st = a->out_stride_t;
   p.out_sh = a->out_stride_h;
   p.lse = a->lse;
-  const size_t o_bytes = (size_t)dev.sm_count * kHeads * 256 * 4;
-  p.ws_o = static_cast<float*>(a->workspace);
-  p.ws_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(a->workspace) + o_bytes);
-  p.flags = reinterpret_cast<int*>(static_cast<uint8_t*>(a->workspace) + o_bytes + (size_t)dev.sm_count * 2 * kHeads * 4);
+  const AttnWorkspace ws = attn_ws_layout(a->workspace, dev.sm_count);
+  p.ws_o = ws.o;
+  p.ws_ml = ws.ml;
+  p.flags = ws.flags;
   p.err = a->error_word;
-  p.epoch = next_epoch(a->workspace);
+  p.epoch = next_attn_epoch(a->workspace);
   p.T = a->T;
   p.NT = (a->topk + C::BN - 1) / C::BN;
   p.U = a->T * C::DV_SPLIT * (int64_t)p.NT;
@@ -1025,8 +1036,6 @@ static dsa_status_t launch(const dsa_attn_args_t* a, const DeviceInfo& dev, cuda
   return e == cudaSuccess ? DSA_OK : cuda_fail(e);
 }
 
-using CfgBf16_256 = AttnCfg<DSA_CACHE_BF16, 256, 0, 1, 112, 3>;
-using CfgFp8_256 = AttnCfg<DSA_CACHE_FP8_SCALED, 256, 0, 1, 112, 3>;
 using CfgBf16_576 = AttnCfg<DSA_CACHE_BF16, 512, 64, 2, 64, 2>;
 using CfgFp8_576 = AttnCfg<DSA_CACHE_FP8_SCALED, 512, 64, 2, 64, 2>;
 
@@ -1070,7 +1079,7 @@ dsa_status_t dsa_sparse_attn_workspace_size(const dsa_attn_args_t* a, size_t* by
   DeviceInfo dev;
   dsa_status_t st = current_device(&dev);
   if (st != DSA_OK) return st;
-  *bytes = ws_bytes_for(dev.sm_count);
+  *bytes = attn_ws_bytes(dev.sm_count);
   return DSA_OK;
 }
 
@@ -1080,12 +1089,9 @@ dsa_status_t dsa_sparse_attn(const dsa_attn_args_t* a, void* stream) {
   DeviceInfo dev;
   st = current_device(&dev);
   if (st != DSA_OK) return st;
-  if (a->workspace_bytes < ws_bytes_for(dev.sm_count)) return DSA_ERR_WORKSPACE_TOO_SMALL;
+  if (a->workspace_bytes < attn_ws_bytes(dev.sm_count)) return DSA_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (a->d_nope == 256) {
-    if (a->kind == DSA_CACHE_BF16) return launch<CfgBf16_256>(a, dev, s);
-    return launch<CfgFp8_256>(a, dev, s);
-  }
+  if (a->d_nope == 256) return launch_attn_k128(a, dev, s);
   if (a->kind == DSA_CACHE_BF16) return launch<CfgBf16_576>(a, dev, s);
   return launch<CfgFp8_576>(a, dev, s);
 }
@@ -1139,7 +1145,7 @@ extern "C" dsa_status_t dsa_sparse_attn_static_ws(const dsa_attn_args_t* a, void
   // at most kStaticWsCtas persistent CTAs: their partials must fit in the fixed array
   DeviceInfo capped = dev;
   if (capped.sm_count > kStaticWsCtas) capped.sm_count = kStaticWsCtas;
-  if (ws_bytes_for(capped.sm_count) > kStaticWsBytes) return DSA_ERR_WORKSPACE_TOO_SMALL;
+  if (attn_ws_bytes(capped.sm_count) > kStaticWsBytes) return DSA_ERR_WORKSPACE_TOO_SMALL;
   void* ws = nullptr;
   st = static_ws_ptr(dev.device, &ws);
   if (st != DSA_OK) return st;
@@ -1148,10 +1154,7 @@ extern "C" dsa_status_t dsa_sparse_attn_static_ws(const dsa_attn_args_t* a, void
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // nothing needs clearing: the array starts zero-filled and each call tags its merge flags
   // with a fresh per-array epoch, so values left by an earlier call never match
-  if (b.d_nope == 256) {
-    if (b.kind == DSA_CACHE_BF16) return launch<CfgBf16_256>(&b, capped, s);
-    return launch<CfgFp8_256>(&b, capped, s);
-  }
+  if (b.d_nope == 256) return launch_attn_k128(&b, capped, s);
   if (b.kind == DSA_CACHE_BF16) return launch<CfgBf16_576>(&b, capped, s);
   return launch<CfgFp8_576>(&b, capped, s);
 }

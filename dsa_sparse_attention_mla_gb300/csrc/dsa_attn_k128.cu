@@ -1,0 +1,1055 @@
+// dsa_attn_k128.cu - DSA sparse MLA attention forward for the 256+0 latent geometry on sm_103a,
+// with the gathered keys as the MMA M dimension.
+//
+// What is computed (sglang PR #38547 "Enable zero-RoPE TileLang DSA on gfx950", Summary and
+// Direct GLM geometry coverage list): for every query token t and head h, gather the latent
+// rows named by t's top-k index list (entries < 0 masked), score s_j = sm_scale * q[t,h].k_j,
+// softmax over j and return sum_j p_j * k_j (all 256 columns: d_v = d_nope, zero RoPE) in
+// bf16. The cache holds bf16 rows or the packed scaled-FP8 rows of the Contract table (256
+// e4m3 codes, then one fp32 scale per 128-column tile).
+//
+// Kernel design (GB300-first, not the pages' TileLang/HIP kernels):
+//  * Transposed products. Scores: S^T[key, head] = K Q^T with M = 128 gathered keys, N = 64
+//    heads, K-dim 256; output: O^T[dv, head] += V^T P^T in two M = 128 halves of d_v, V^T read
+//    MN-major from the same K tile and P^T MN-major (one 128-byte row of 64 head weights per
+//    key). tcgen05 kind::f16, bf16 operands, fp32 accumulators in tensor memory with lane =
+//    key (scores) or lane = output column (O). M = 128 keeps the tensor core at full width,
+//    where heads as M (M = 64) would use half of it.
+//  * Packed FP8 rows are widened to bf16 exactly and without their scales. The two tile scales
+//    belong to one key, i.e. one accumulator lane, so they are applied in fp32 where that lane
+//    is read: the score is sc0 * S_0 + sc1 * S_1 (S_t accumulates the columns of tile t), and
+//    the probabilities that multiply tile t of V are p * sc_t (two P buffers, one per tile).
+//  * Softmax per key: one thread per TMEM lane holds its key's 64 scores. The running max of
+//    each head (exp2 domain) lives in shared memory and is raised only when a tile exceeds it by
+//    more than 2^8 (a CTA-wide vote of the four softmax warps); the first tile of a segment
+//    takes exact per-head maxima with warp max-reductions. Partial row sums per lane accumulate
+//    in TMEM and are reduced across lanes once per token.
+//  * Persistent cooperative launch, one CTA per SM; (token, 128-position tile) units split into
+//    contiguous ranges per CTA; a token cut by a range boundary is merged in-kernel by the CTA
+//    holding its first tiles (fixed order, no atomics on data).
+//  * Warp roles: 0 producer (index read, -1 compaction into dense 128-key tiles, page
+//    translation, L2 prefetch of packed rows, Q loads by TMA), 1 score-MMA issuer, 2 output-MMA
+//    issuer, 4-7 softmax and epilogue, 8-15 row loaders (cp.async copies of bf16 rows, or loads
+//    of packed rows widened into the 128-byte-swizzled K tile); warp 3 idle.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "dsa_attn_common.h"
+#include "dsa_host.h"
+#include "dsa_ptx.cuh"
+
+namespace dsa {
+namespace k128 {
+
+constexpr int kH = kAttnHeads;  // heads: MMA N
+constexpr int kD = 256;         // latent width (= d_v)
+constexpr int kBN = 128;        // gathered keys per tile: MMA M
+constexpr int kKST = 2;         // K tile stages
+constexpr int kMST = 8;         // meta ring depth
+constexpr int kNLD = 8;         // loader warps
+constexpr int kWarps = 8 + kNLD;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kRPW = kBN / kNLD;  // rows per loader warp per tile
+constexpr int kMaxParts = 32;     // most parts of one split token (the launch guarantees it)
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+template <int KIND>
+struct Cfg {
+  static constexpr bool FP8 = KIND == DSA_CACHE_FP8_SCALED;
+  static constexpr int RB = FP8 ? 264 : 512;  // cache row bytes
+  static constexpr int NSUB = FP8 ? 2 : 1;    // score accumulators per tile (one per scale tile)
+  static constexpr int PBUF = FP8 ? 1 : 2;    // P buffers
+  static constexpr int P_BYTES = NSUB * kBN * 128;
+  // shared memory carve-up (offsets from a 1024-aligned base)
+  static constexpr int Q_OFF = 0;
+  static constexpr int Q_BYTES = kH * kD * 2;
+  static constexpr int KT_OFF = Q_OFF + Q_BYTES;
+  static constexpr int KT_BYTES = kBN * kD * 2;
+  static constexpr int P_OFF = KT_OFF + kKST * KT_BYTES;
+  static constexpr int SC_OFF = P_OFF + PBUF * P_BYTES;
+  static constexpr int SC_BYTES = FP8 ? kBN * 8 : 0;  // per stage: (scale0, scale1) per row
+  static constexpr int META_OFF = SC_OFF + kKST * SC_BYTES;
+  static constexpr int META_BYTES = 32 + 4 * kBN;
+  static constexpr int CMP_OFF = META_OFF + kMST * META_BYTES;  // producer: one step's valid slots
+  static constexpr int RED_OFF = CMP_OFF + 4 * 256;
+  // m[64], alpha[64], lsum[64], spare[64], part[4][64], wk[kMaxParts][64], votes[2][4]
+  static constexpr int RED_FLOATS = 8 * kH + kMaxParts * kH + 8;
+  static constexpr int BAR_OFF = RED_OFF + ((RED_FLOATS * 4 + 15) & ~15);
+  static constexpr int NBARS = 2 + 2 * kKST + 2 * kMST + 8 + 3;
+  static constexpr int MISC_OFF = BAR_OFF + 8 * NBARS;
+  static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + alignment slack
+  // tensor memory columns
+  static constexpr int S_COLS = 64 * NSUB;  // per S buffer (two buffers)
+  static constexpr int O_COL = 2 * S_COLS;  // O^T halves: dv 0-127 at O_COL, dv 128-255 at O_COL + 64
+  static constexpr int L_COL = O_COL + 128;
+  static constexpr int TMEM_COLS = 512;
+  static_assert(L_COL + 64 <= TMEM_COLS, "TMEM budget");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(KT_OFF % 1024 == 0 && P_OFF % 1024 == 0 && KT_BYTES % 1024 == 0, "operand alignment");
+};
+
+// meta ring entry types and segment kinds
+enum : int { kTile = 1, kSegEnd = 2, kDone = 3 };
+enum : int { kComplete = 0, kHead = 1, kPart = 2 };
+
+struct MetaHdr {
+  int type;
+  int token;
+  int n_valid;     // kTile: valid rows in this tile
+  int first;       // kTile: first non-empty tile of its segment
+  int kind;        // kSegEnd: segment kind
+  int had_tiles;   // kSegEnd: the segment had at least one non-empty tile
+  int merge_last;  // kSegEnd: last CTA holding a part of this token
+  int pad;
+};
+
+struct Params {
+  const uint8_t* cache;
+  int64_t num_slots;
+  const int32_t* idx;
+  int64_t idx_stride;
+  int topk;
+  const int32_t* bt;
+  int64_t bt_stride;
+  int page_size;
+  int max_pages;
+  uint32_t pg_mul;  // x / page_size == (x * pg_mul) >> pg_shift for 0 <= x < 2^31
+  int pg_shift;
+  const int32_t* req;
+  float c_log2;  // sm_scale * log2(e)
+  uint16_t* out;
+  int64_t out_st, out_sh;
+  float* lse;
+  float* ws_o;   // [G][256 dv][64 heads] partial O^T (unnormalised, relative to its max)
+  float* ws_ml;  // [G][2][64] partial max (exp2 domain) and row sum
+  int* flags;    // [G][4] partial published (holds the call's epoch), one per softmax warp
+  int epoch;
+  int32_t* err;
+  int64_t T;
+  int NT;     // 128-position tiles per token (over the index width)
+  int64_t U;  // total units = T * NT
+  int G;      // CTAs
+};
+
+__device__ __forceinline__ void set_err(int32_t* err, int bits) {
+  if (err) atomicOr(err, bits);
+}
+__device__ __forceinline__ int64_t unit_begin(int64_t b, int64_t U, int G) { return (b * U) / G; }
+__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+__device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
+
+// Exchange among the four softmax warps (one arrival each on `xbar`, phase `n` of it): returns
+// the OR of `v` over the warps, with every warp's earlier shared-memory writes visible, or -1
+// when a warp did not arrive within the time limit.
+static __device__ __noinline__ int softmax_exchange(uint32_t xbar, int* votes, uint32_t n, int sp, int v) {
+  const int lane = threadIdx.x & 31;
+  const int slot = n & 1;
+  const bool any = __any_sync(0xffffffffu, v != 0);
+  if (lane == 0) votes[slot * 4 + sp] = any ? 1 : 0;
+  __syncwarp();
+  if (lane == 0) mbar_arrive(xbar);
+  const bool ok = mbar_wait(xbar, n & 1, kWaitNs);
+  if (!__all_sync(0xffffffffu, ok)) return -1;
+  return (votes[slot * 4] | votes[slot * 4 + 1] | votes[slot * 4 + 2] | votes[slot * 4 + 3]) ? 1 : 0;
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_k128_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmap_q) {
+  using C = Cfg<KIND>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const uint32_t bar0 = sbase + C::BAR_OFF;
+  const uint32_t q_full = bar0, q_empty = bar0 + 8;
+  auto k_full = [&](int s) { return bar0 + 16 + 8 * s; };
+  auto k_empty = [&](int s) { return bar0 + 16 + 8 * (kKST + s); };
+  auto m_full = [&](int s) { return bar0 + 16 + 8 * (2 * kKST + s); };
+  auto m_empty = [&](int s) { return bar0 + 16 + 8 * (2 * kKST + kMST + s); };
+  const uint32_t x0 = bar0 + 16 + 8 * (2 * kKST + 2 * kMST);
+  auto s_full = [&](int i) { return x0 + 8 * i; };
+  auto s_empty = [&](int i) { return x0 + 16 + 8 * i; };
+  auto p_full = [&](int i) { return x0 + 32 + 8 * i; };
+  auto pv_done = [&](int i) { return x0 + 48 + 8 * i; };
+  const uint32_t xbar = x0 + 64;        // softmax-warp exchange (4 arrivals per phase)
+  const uint32_t mma_drain = x0 + 72;   // every MMA of an issuer complete (x0 + 72: scores, + 80: output)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int s = 0; s < kKST; ++s) {
+      // bf16 rows: one cp.async arrive per loader thread; packed rows: one arrive per loader warp
+      mbar_init(k_full(s), C::FP8 ? kNLD : 32 * kNLD);
+      mbar_init(k_empty(s), 1);
+    }
+    for (int s = 0; s < kMST; ++s) {
+      mbar_init(m_full(s), 1);
+      mbar_init(m_empty(s), 2 + 4 + kNLD);  // 2 MMA threads, 4 softmax, loader warps
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(s_full(i), 1);
+      mbar_init(s_empty(i), 4);
+      mbar_init(p_full(i), 4);
+      mbar_init(pv_done(i), 1);
+    }
+    mbar_init(xbar, 4);
+    mbar_init(mma_drain, 1);
+    mbar_init(mma_drain + 8, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) prefetch_tmap(&tmap_q);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int b = blockIdx.x;
+
+  auto fail = [&](int bits) {
+    set_err(p.err, bits);
+    *abort_flag = 1;
+  };
+  auto wait = [&](uint32_t bar, uint32_t par) -> bool {
+    if (mbar_wait(bar, par, kWaitNs)) return true;
+    fail(DSA_DEVERR_TIMEOUT);
+    return false;
+  };
+
+  if (warp == 0) {
+    // =========================================================== producer (one warp) ====
+    // Walks this CTA's unit range segment by segment. The index window of a segment is read 256
+    // entries per step (two steps ahead, block-table rows one step ahead); entries < 0 are
+    // dropped and the valid ones packed, in index order, into dense 128-key tiles, so runs of
+    // padding cost only their index reads and every emitted tile but a segment's last is full.
+    uint32_t mc = 0, qc = 0;
+    const int64_t u0 = unit_begin(b, p.U, p.G), u1 = unit_begin(b + 1, p.U, p.G);
+    auto emit_begin = [&](int& st) -> MetaHdr* {
+      st = mc % kMST;
+      if (mc >= (uint32_t)kMST) wait(m_empty(st), ((mc / kMST) & 1) ^ 1);
+      return reinterpret_cast<MetaHdr*>(smem + C::META_OFF + st * C::META_BYTES);
+    };
+    auto emit_end = [&](int st) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(m_full(st));
+      ++mc;
+    };
+    const int64_t pos_limit = p.bt ? (int64_t)p.max_pages * p.page_size : p.num_slots;
+    int64_t u = u0;
+    int64_t t = u0 / p.NT;       // token and tile of the CTA's first unit; later segments start
+    int j0 = (int)(u0 - t * p.NT);  // at tile 0 of the next token
+    while (u < u1 && !*abort_flag) {
+      const int j1 = (int)((int64_t)(p.NT - j0) < u1 - u ? p.NT : j0 + (u1 - u));
+      const int64_t uend = u + (j1 - j0);
+      const int kind = j0 > 0 ? kPart : (j1 < p.NT ? kHead : kComplete);
+      const int64_t req = p.req ? p.req[t] : 0;
+      const int32_t* irow = p.idx + t * p.idx_stride;
+      const int32_t* btrow = p.bt ? p.bt + req * p.bt_stride : nullptr;
+      const int e0 = j0 * kBN, e1 = min(j1 * kBN, p.topk);
+      {  // pull this segment's index window and the request's block-table row into L2
+        const uintptr_t a0 = reinterpret_cast<uintptr_t>(irow + e0) & ~uintptr_t(127);
+        const uintptr_t a1 = reinterpret_cast<uintptr_t>(irow + e1);
+        for (uintptr_t a = a0 + 128 * lane; a < a1; a += 32 * 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+        if (btrow) {
+          const uintptr_t c0 = reinterpret_cast<uintptr_t>(btrow) & ~uintptr_t(127);
+          const uintptr_t c1 = reinterpret_cast<uintptr_t>(btrow + p.max_pages);
+          for (uintptr_t a = c0 + 128 * lane; a < c1; a += 32 * 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+        }
+      }
+      constexpr int V = 4;
+      auto load_step = [&](int pos, int (&v)[V]) {
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+          const int e = pos + 32 * k + lane;
+          v[k] = e < e1 ? __ldg(irow + e) : -1;
+        }
+      };
+      auto page_of = [&](const int (&x)[V], int (&pg)[V]) {
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+          if (x[k] < 0) pg[k] = -1;
+          else if (x[k] >= pos_limit) pg[k] = -2;
+          else pg[k] = btrow ? __ldg(btrow + (int)(((uint64_t)(uint32_t)x[k] * p.pg_mul) >> p.pg_shift)) : x[k];
+        }
+      };
+      int ia[V], ib[V], pa[V];
+      load_step(e0, ia);
+      load_step(e0 + 32 * V, ib);
+      page_of(ia, pa);
+      bool had = false, open = false;
+      int cnt = 0, st = 0;
+      int* slots = nullptr;
+      MetaHdr* mh = nullptr;
+      auto open_tile = [&]() {
+        if (!had) {  // Q of this segment, loaded with its first tile
+          if (qc > 0) wait(q_empty, (qc - 1) & 1);
+          if (lane == 0) mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+          __syncwarp();
+          if (lane < kD / 64)
+            tma_load_3d(sbase + C::Q_OFF + lane * (kH * 128), &tmap_q, 64 * lane, 0, (int)t, q_full);
+          ++qc;
+        }
+        mh = emit_begin(st);
+        slots = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(mh) + 32);
+        if (lane == 0) {
+          mh->type = kTile;
+          mh->token = (int)t;
+          mh->first = had ? 0 : 1;
+        }
+        had = true;
+        open = true;
+        cnt = 0;
+      };
+      auto close_tile = [&](int n) {
+        if (lane == 0) mh->n_valid = n;
+        emit_end(st);
+        open = false;
+      };
+      int* cbuf = reinterpret_cast<int*>(smem + C::CMP_OFF);
+      for (int pos = e0; pos < e1 && !*abort_flag; pos += 32 * V) {
+        int ic[V], pb[V];
+        load_step(pos + 64 * V, ic);
+        page_of(ib, pb);
+        // compact this step's valid slots, in index order, into cbuf
+        int bad = 0, nstep = 0;
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+          int64_t slot = -1;
+          if (pa[k] >= 0) {
+            if (btrow) {
+              const int pq = (int)(((uint64_t)(uint32_t)ia[k] * p.pg_mul) >> p.pg_shift);
+              slot = (int64_t)pa[k] * p.page_size + (ia[k] - pq * p.page_size);
+              if (slot >= p.num_slots) slot = -2;
+            } else {
+              slot = pa[k];
+            }
+          } else if (pa[k] == -2 || (btrow && ia[k] >= 0)) {
+            slot = -2;  // outside the addressable range, or a negative block-table page
+          }
+          bad |= (slot == -2);
+          const bool ok = slot >= 0;
+          const uint32_t bal = __ballot_sync(0xffffffffu, ok);
+          if (ok) cbuf[nstep + __popc(bal & ((1u << lane) - 1u))] = (int)slot;
+          if constexpr (C::FP8) {
+            // pull the packed row into L2 a few tiles before the loaders read it (one LSU
+            // prefetch per 128-byte line it touches)
+            if (ok) {
+              const uintptr_t r0 = reinterpret_cast<uintptr_t>(p.cache + slot * C::RB);
+              for (uintptr_t a = r0 & ~uintptr_t(127); a < r0 + C::RB; a += 128)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(a > r0 ? a : r0));
+            }
+          }
+          nstep += __popc(bal);
+        }
+        if (bad) set_err(p.err, DSA_DEVERR_INDEX_OUT_OF_RANGE);
+        __syncwarp();
+        // move them into dense tiles of kBN keys
+        for (int c = 0; c < nstep;) {
+          if (!open) open_tile();
+          const int take = min(kBN - cnt, nstep - c);
+          for (int i = lane; i < take; i += 32) slots[cnt + i] = cbuf[c + i];
+          cnt += take;
+          c += take;
+          if (cnt == kBN) close_tile(kBN);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+          ia[k] = ib[k];
+          ib[k] = ic[k];
+          pa[k] = pb[k];
+        }
+      }
+      if (open) close_tile(cnt);
+      {
+        int st2;
+        MetaHdr* me = emit_begin(st2);
+        if (lane == 0) {
+          me->type = kSegEnd;
+          me->token = (int)t;
+          me->kind = kind;
+          me->had_tiles = had ? 1 : 0;
+          int last = b;
+          if (kind == kHead) {
+            // the last CTA c whose range starts at or before the token's last unit L:
+            // floor(c * U / G) <= L  <=>  c <= ceil((L + 1) * G / U) - 1
+            const int64_t L1 = (t + 1) * p.NT;
+            const int64_t c = (L1 * p.G + p.U - 1) / p.U - 1;
+            last = (int)(c < p.G - 1 ? c : p.G - 1);
+          }
+          me->merge_last = last;
+        }
+        emit_end(st2);
+      }
+      u = uend;
+      ++t;
+      j0 = 0;
+    }
+    {
+      int st;
+      MetaHdr* mh = emit_begin(st);
+      if (lane == 0) mh->type = kDone;
+      emit_end(st);
+    }
+    // no Q copy may still be in flight when the CTA exits
+    if (qc > 0) mbar_wait(q_full, (qc - 1) & 1, kWaitNs);
+  } else if (warp == 1 || warp == 2) {
+    // ======================================================= MMA issuers (2 threads) ====
+    // Warp 1 issues the score products, warp 2 the output products. Each is a short blocking
+    // loop over the meta ring, so a tile whose probabilities are ready never waits behind the
+    // next tile's score product (the tensor core takes both streams; their accumulators are
+    // disjoint). Every MMA is straight-line code: one 32-bit add on each descriptor's low word.
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(128, kH, 0, 0);   // A = K tile (K-major), B = Q (K-major)
+      constexpr uint32_t idPV = idesc_bf16(128, kH, 1, 1);  // A = V^T (MN-major), B = P^T (MN-major)
+      const uint64_t dq = sw128_desc(sbase + C::Q_OFF, 16, 1024);
+      const uint32_t q_lo = (uint32_t)dq, q_hi = (uint32_t)(dq >> 32);
+      const uint32_t k_hi = (uint32_t)(sw128_desc(0, 16, 1024) >> 32);
+      const uint32_t mn_hi = (uint32_t)(sw128_desc(0, kBN * 128, 1024) >> 32);
+      uint32_t mc = 0, g = 0, qc = 0;
+      for (;;) {
+        const int st = mc % kMST;
+        if (!wait(m_full(st), (mc / kMST) & 1)) break;
+        const MetaHdr* mh = reinterpret_cast<const MetaHdr*>(smem + C::META_OFF + st * C::META_BYTES);
+        const int type = mh->type;
+        const int first = mh->first, had = mh->had_tiles;
+        mbar_arrive(m_empty(st));
+        ++mc;
+        if (type == kDone) break;
+        if (type == kSegEnd) {
+          // the segment's score products are all issued: its Q buffer is free once they complete
+          if (warp == 1 && had) mma_commit(q_empty);
+          continue;
+        }
+        const int ks = g % kKST;
+        if (warp == 1) {
+          // ---- scores S^T = K Q^T for tile g (two 64-column sub-accumulators for packed rows)
+          if (first) {
+            if (!wait(q_full, qc & 1)) break;
+            ++qc;
+          }
+          if (!wait(k_full(ks), (g / kKST) & 1)) break;
+          if (g >= 2 && !wait(s_empty(g & 1), ((g >> 1) & 1) ^ 1)) break;
+          // bf16 rows arrive by cp.async (generic proxy): order them before the tensor core reads
+          // (the packed-row loaders fence on their side before arriving)
+          if constexpr (!C::FP8) fence_proxy_async_smem();
+          tc_fence_after();
+          const uint32_t k_lo = (uint32_t)sw128_desc(sbase + C::KT_OFF + ks * C::KT_BYTES, 16, 1024);
+          const uint32_t d0 = tmem + (g & 1) * C::S_COLS;
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            // 16-column step kk: chunk kk/4 of 64 columns, 32 bytes per step inside the chunk
+            const uint32_t ka = (uint32_t)((kk >> 2) * ((kBN * 128) >> 4) + (kk & 3) * 2);
+            const uint32_t qa = (uint32_t)((kk >> 2) * ((kH * 128) >> 4) + (kk & 3) * 2);
+            // packed rows: columns 0-127 and 128-255 accumulate separately (one scale each)
+            const uint32_t d = C::FP8 ? d0 + 64 * (kk >> 3) : d0;
+            if ((C::FP8 ? (kk & 7) : kk) == 0) mma_bf16_lohi<0>(d, k_lo + ka, k_hi, q_lo + qa, q_hi, idS);
+            else mma_bf16_lohi<1>(d, k_lo + ka, k_hi, q_lo + qa, q_hi, idS);
+          }
+          mma_commit(s_full(g & 1));
+        } else {
+          // ---- output O^T += V^T P^T for tile g, once its probabilities are written
+          if (!wait(p_full(g % C::PBUF), (g / C::PBUF) & 1)) break;
+          tc_fence_after();
+          // V^T: 64-column groups of the K tile are 128 * 128 bytes apart (LBO), 8-key groups 1024
+          const uint32_t v_lo = (uint32_t)sw128_desc(sbase + C::KT_OFF + ks * C::KT_BYTES, kBN * 128, 1024);
+          const uint32_t p_lo = (uint32_t)sw128_desc(sbase + C::P_OFF + (g % C::PBUF) * C::P_BYTES, kBN * 128, 1024);
+          // output columns 128h .. 128h + 127 (V^T two 64-column groups further); 16 keys per
+          // step (16 rows of 128 bytes); packed rows take p * scale of tile h
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t d = tmem + C::O_COL + 64 * h;
+            const uint32_t va = v_lo + h * ((2 * kBN * 128) >> 4);
+            const uint32_t pa = p_lo + (C::FP8 ? h * ((kBN * 128) >> 4) : 0);
+            // the first step of a segment's first tile overwrites the accumulator
+            mma_bf16(d, ((uint64_t)mn_hi << 32) | va, ((uint64_t)mn_hi << 32) | pa, idPV, first ? 0u : 1u);
+#pragma unroll
+            for (int j = 1; j < kBN / 16; ++j) mma_bf16_lohi<1>(d, va + 128 * j, mn_hi, pa + 128 * j, mn_hi, idPV);
+          }
+          mma_commit(k_empty(ks));
+          mma_commit(pv_done(g & 1));
+        }
+        ++g;
+      }
+      // drain: every MMA issued by this thread completes before TMEM can be released
+      const uint32_t drain = warp == 1 ? mma_drain : mma_drain + 8;
+      mma_commit(drain);
+      mbar_wait(drain, 0, kWaitNs);
+    }
+    __syncwarp();
+  } else if (warp >= 4 && warp < 8) {
+    // =============================================== softmax + epilogue (4 warps) ====
+    const int sp = warp & 3;                                 // TMEM lane quarter
+    const int tr = 32 * sp + lane;                           // key row of the tile / dv row of O^T
+    const uint32_t tl = tmem + ((uint32_t)(32 * sp) << 16);  // this warp's lanes
+    float* red = reinterpret_cast<float*>(smem + C::RED_OFF);
+    float* red_m = red;           // running max per head (exp2 domain)
+    float* red_alpha = red + 64;  // rescale factor per head; epilogue: weight of own partial
+    float* red_part = red + 256;  // [4 warps][64 heads]
+    float* red_wk = red + 512;    // [kMaxParts][64]: merge weights of the other parts
+    int* votes = reinterpret_cast<int*>(red + 512 + kMaxParts * kH);  // [2][4]
+    uint32_t mc = 0, g = 0, xc = 0;
+    auto xsync = [&](bool v) -> int {
+      const int r = softmax_exchange(xbar, votes, xc++, sp, v ? 1 : 0);
+      if (r < 0) fail(DSA_DEVERR_TIMEOUT);
+      return r;
+    };
+    auto wait_all = [&](bool ok) -> bool {
+      if (__all_sync(0xffffffffu, ok)) return true;
+      fail(DSA_DEVERR_TIMEOUT);
+      return false;
+    };
+    for (;;) {
+      const int st = mc % kMST;
+      if (!wait_all(mbar_wait(m_full(st), (mc / kMST) & 1, kWaitNs))) break;
+      const MetaHdr* mh = reinterpret_cast<const MetaHdr*>(smem + C::META_OFF + st * C::META_BYTES);
+      const int type = mh->type;
+      if (type == kDone) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(m_empty(st));
+        break;
+      }
+      if (type == kTile) {
+        const int n_valid = mh->n_valid;
+        const int first = mh->first;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(m_empty(st));
+        ++mc;
+        const int ks = g % kKST;
+        bool ok = mbar_wait(s_full(g & 1), (g >> 1) & 1, kWaitNs);
+        // the tile scales come from the loaders: acquire their stage barrier directly
+        if constexpr (C::FP8) ok = ok && mbar_wait(k_full(ks), (g / kKST) & 1, kWaitNs);
+        if (!wait_all(ok)) break;
+        tc_fence_after();
+        const bool valid = tr < n_valid;
+        float sc0 = 1.0f, sc1 = 0.0f;
+        if constexpr (C::FP8) {
+          const float2 sc = *reinterpret_cast<const float2*>(smem + C::SC_OFF + ks * C::SC_BYTES + tr * 8);
+          sc0 = sc.x;
+          sc1 = sc.y;
+        }
+        const float c0 = p.c_log2 * sc0, c1 = p.c_log2 * sc1;
+        const uint32_t sa = tl + (g & 1) * C::S_COLS;
+        // score of head i of a chunk, exp2 domain, before subtracting the running max
+        auto score = [&](const uint32_t (&a)[16], const uint32_t (&bb)[16], int i) -> float {
+          if constexpr (C::FP8) return fmaf(u2f(a[i]), c0, u2f(bb[i]) * c1);
+          else return u2f(a[i]) * c0;
+        };
+        bool slow = first != 0;
+        if (!slow) {
+          // does any valid key exceed its head's running max by more than 2^8?
+          float xm = -INFINITY;
+#pragma unroll 1
+          for (int ch = 0; ch < 4; ++ch) {
+            uint32_t a[16], bb[16];
+            tmem_ld32_x16(sa + 16 * ch, a);
+            if constexpr (C::FP8) tmem_ld32_x16(sa + 64 + 16 * ch, bb);
+            tc_wait_ld();
+            const float* mrow = red_m + 16 * ch;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) xm = fmaxf(xm, score(a, bb, i) - mrow[i]);
+          }
+          const int r = xsync(valid && xm > 8.0f);
+          if (r < 0) break;
+          slow = r != 0;
+        }
+        bool resc = false;
+        if (slow) {
+          // exact per-head maximum of this tile: warp max-reductions, then across the 4 warps
+#pragma unroll 1
+          for (int ch = 0; ch < 4; ++ch) {
+            uint32_t a[16], bb[16];
+            tmem_ld32_x16(sa + 16 * ch, a);
+            if constexpr (C::FP8) tmem_ld32_x16(sa + 64 + 16 * ch, bb);
+            tc_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int mx = redux_max_s32(f2ord(valid ? score(a, bb, i) : -INFINITY));
+              if (lane == ((16 * ch + i) & 31)) red_part[sp * 64 + 16 * ch + i] = ord2f(mx);
+            }
+          }
+          if (xsync(false) < 0) break;
+          bool grow_any = false;
+          if (tr < kH) {
+            const float mt =
+                fmaxf(fmaxf(red_part[tr], red_part[64 + tr]), fmaxf(red_part[128 + tr], red_part[192 + tr]));
+            const float mo = first ? -INFINITY : red_m[tr];
+            const bool grow = first || mt > mo + 8.0f;
+            const float mn = grow ? mt : mo;
+            red_alpha[tr] = grow ? ex2_approx(mo - mn) : 1.0f;
+            red_m[tr] = mn;
+            grow_any = grow && !first;
+          }
+          const int r = xsync(grow_any);
+          if (r < 0) break;
+          resc = r != 0;
+        }
+        // the P buffer must be free; a rescale also needs every issued PV complete
+        ok = true;
+        if (g >= (uint32_t)C::PBUF) ok = mbar_wait(pv_done((g - C::PBUF) & 1), ((g - C::PBUF) >> 1) & 1, kWaitNs);
+        if (resc && C::PBUF > 1 && g >= 1) ok = ok && mbar_wait(pv_done((g - 1) & 1), ((g - 1) >> 1) & 1, kWaitNs);
+        if (!wait_all(ok)) break;
+        tc_fence_after();
+        if (resc) {  // rare: some head's max grew; scale its O^T column and partial sums
+#pragma unroll 1
+          for (int ch = 0; ch < 4; ++ch) {
+            uint32_t o0[16], o1[16], l[16];
+            tmem_ld32_x16(tl + C::O_COL + 16 * ch, o0);
+            tmem_ld32_x16(tl + C::O_COL + 64 + 16 * ch, o1);
+            tmem_ld32_x16(tl + C::L_COL + 16 * ch, l);
+            tc_wait_ld();
+            const float* al = red_alpha + 16 * ch;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float a = al[i];
+              o0[i] = f2u(u2f(o0[i]) * a);
+              o1[i] = f2u(u2f(o1[i]) * a);
+              l[i] = f2u(u2f(l[i]) * a);
+            }
+            tmem_st32_x16(tl + C::O_COL + 16 * ch, o0);
+            tmem_st32_x16(tl + C::O_COL + 64 + 16 * ch, o1);
+            tmem_st32_x16(tl + C::L_COL + 16 * ch, l);
+          }
+        }
+        // probabilities: one FFMA and one MUFU ex2 per score; row sums into TMEM; P (or, for
+        // packed rows, p * scale of each tile) as bf16 into this key's 128-byte row
+        uint8_t* prow = smem + C::P_OFF + (g % C::PBUF) * C::P_BYTES + tr * 128;
+        const int sw = tr & 7;
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t a[16], bb[16], l[16];
+          tmem_ld32_x16(sa + 16 * ch, a);
+          if constexpr (C::FP8) tmem_ld32_x16(sa + 64 + 16 * ch, bb);
+          tmem_ld32_x16(tl + C::L_COL + 16 * ch, l);
+          tc_wait_ld();
+          const float* mrow = red_m + 16 * ch;
+          float pr[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            pr[i] = valid ? ex2_approx(score(a, bb, i) - mrow[i]) : 0.0f;
+            l[i] = f2u(first ? pr[i] : u2f(l[i]) + pr[i]);
+          }
+          tmem_st32_x16(tl + C::L_COL + 16 * ch, l);
+          uint32_t w[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) w[i] = f32x2_to_bf16x2(pr[2 * i] * sc0, pr[2 * i + 1] * sc0);
+          *reinterpret_cast<uint4*>(prow + (((2 * ch) ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(prow + (((2 * ch + 1) ^ sw) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+          if constexpr (C::FP8) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) w[i] = f32x2_to_bf16x2(pr[2 * i] * sc1, pr[2 * i + 1] * sc1);
+            *reinterpret_cast<uint4*>(prow + kBN * 128 + (((2 * ch) ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(prow + kBN * 128 + (((2 * ch + 1) ^ sw) << 4)) =
+                make_uint4(w[4], w[5], w[6], w[7]);
+          }
+        }
+        fence_proxy_async_smem();
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(p_full(g % C::PBUF));
+          mbar_arrive(s_empty(g & 1));
+        }
+        ++g;
+        continue;
+      }
+      // ====================================================== kSegEnd: token epilogue ====
+      const int64_t t = mh->token;
+      const int kind = mh->kind, had = mh->had_tiles, last = mh->merge_last;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(m_empty(st));
+      ++mc;
+      if (had) {
+        if (!wait_all(mbar_wait(pv_done((g - 1) & 1), ((g - 1) >> 1) & 1, kWaitNs))) break;
+        tc_fence_after();
+      }
+      // row sums: each lane's 64 partial sums go to its row of a [128][64] fp32 block in the (idle)
+      // P buffers, 16-byte granule q of row r at ((q ^ (r & 15)) << 4); then thread h < 64 adds up
+      // column h (conflict-free: a warp reads 32 consecutive columns of one row)
+      float* lrow = reinterpret_cast<float*>(smem + C::P_OFF);
+      {
+        float* dst = lrow + tr * kH;
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t l[16];
+          if (had) {
+            tmem_ld32_x16(tl + C::L_COL + 16 * ch, l);
+            tc_wait_ld();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) l[i] = 0u;
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(dst + ((((4 * ch + q) ^ (tr & 15))) << 2)) =
+                make_uint4(l[4 * q], l[4 * q + 1], l[4 * q + 2], l[4 * q + 3]);
+        }
+      }
+      if (xsync(false) < 0) break;
+      if (tr < kH) {
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 4
+        for (int r = 0; r < kBN; ++r) acc[r & 3] += lrow[r * kH + ((((tr >> 2) ^ (r & 15))) << 2) + (tr & 3)];
+        red_part[tr] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+      }
+      if (xsync(false) < 0) break;
+      float lsum = 0.0f, mrow = -INFINITY;
+      if (tr < kH && had) {
+        lsum = red_part[tr];
+        mrow = red_m[tr];
+      }
+      if (kind == kPart) {
+        // publish (O^T, m, l) of this part in workspace slot b
+        if (tr < kH) {
+          p.ws_ml[((int64_t)b * 2 + 0) * kH + tr] = mrow;
+          p.ws_ml[((int64_t)b * 2 + 1) * kH + tr] = lsum;
+        }
+        if (had) {
+          float* w0 = p.ws_o + ((int64_t)b * kD + tr) * kH;
+          float* w1 = p.ws_o + ((int64_t)b * kD + 128 + tr) * kH;
+#pragma unroll 1
+          for (int ch = 0; ch < 4; ++ch) {
+            uint32_t o0[16], o1[16];
+            tmem_ld32_x16(tl + C::O_COL + 16 * ch, o0);
+            tmem_ld32_x16(tl + C::O_COL + 64 + 16 * ch, o1);
+            tc_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) {
+              *reinterpret_cast<float4*>(w0 + 16 * ch + i) = make_float4(u2f(o0[i]), u2f(o0[i + 1]), u2f(o0[i + 2]), u2f(o0[i + 3]));
+              *reinterpret_cast<float4*>(w1 + 16 * ch + i) = make_float4(u2f(o1[i]), u2f(o1[i + 1]), u2f(o1[i + 2]), u2f(o1[i + 3]));
+            }
+          }
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0)
+          asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.flags + 4 * b + sp), "r"(p.epoch) : "memory");
+        tc_fence_before();
+        continue;
+      }
+      // complete token, or the head of a split token: merge parts b+1 .. last in order
+      const int nparts = kind == kHead ? last - b : 0;
+      bool okp = true;
+      for (int k = 1; k <= nparts && okp; ++k) {
+        for (int j = 0; j < 4 && okp; ++j) {
+          int v = 0;
+          const uint64_t t0 = globaltimer_ns();
+          for (;;) {
+            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p.flags + 4 * (b + k) + j) : "memory");
+            if (v == p.epoch || globaltimer_ns() - t0 > kWaitNs) break;
+            __nanosleep(64);
+          }
+          okp = v == p.epoch;
+        }
+      }
+      if (!okp) fail(DSA_DEVERR_TIMEOUT);
+      // (the launch keeps nparts <= kMaxParts; more would overrun the weight table)
+      const int np = (okp && nparts <= kMaxParts) ? nparts : 0;
+      if (tr < kH) {
+        float M = mrow;
+        for (int k = 1; k <= np; ++k) M = fmaxf(M, p.ws_ml[((int64_t)(b + k) * 2 + 0) * kH + tr]);
+        const float w_own = lsum > 0.0f ? exp2f(mrow - M) : 0.0f;
+        float L = w_own * lsum;
+        for (int k = 1; k <= np; ++k) {
+          const float mk = p.ws_ml[((int64_t)(b + k) * 2 + 0) * kH + tr];
+          const float lk = p.ws_ml[((int64_t)(b + k) * 2 + 1) * kH + tr];
+          const float wk = lk > 0.0f ? exp2f(mk - M) : 0.0f;
+          red_wk[(k - 1) * kH + tr] = wk;
+          L += wk * lk;
+        }
+        const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+        red_alpha[tr] = w_own * inv;
+        for (int k = 1; k <= np; ++k) red_wk[(k - 1) * kH + tr] *= inv;
+        if (p.lse) p.lse[t * kH + tr] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+      }
+      if (xsync(false) < 0) break;
+      // combine and stage the bf16 block [64 heads][256 columns] in the (idle) P buffers
+      uint16_t* stage = reinterpret_cast<uint16_t*>(smem + C::P_OFF);
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        float acc0[16], acc1[16];
+        const float* wo = red_alpha + 16 * ch;
+        if (had) {
+          uint32_t o0[16], o1[16];
+          tmem_ld32_x16(tl + C::O_COL + 16 * ch, o0);
+          tmem_ld32_x16(tl + C::O_COL + 64 + 16 * ch, o1);
+          tc_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            acc0[i] = wo[i] * u2f(o0[i]);
+            acc1[i] = wo[i] * u2f(o1[i]);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) acc0[i] = acc1[i] = 0.0f;
+        }
+        for (int k = 1; k <= np; ++k) {
+          const float* wk = red_wk + (k - 1) * kH + 16 * ch;
+          const float* s0 = p.ws_o + ((int64_t)(b + k) * kD + tr) * kH + 16 * ch;
+          const float* s1 = p.ws_o + ((int64_t)(b + k) * kD + 128 + tr) * kH + 16 * ch;
+#pragma unroll
+          for (int i = 0; i < 16; i += 4) {
+            const float4 x = *reinterpret_cast<const float4*>(s0 + i);
+            const float4 y = *reinterpret_cast<const float4*>(s1 + i);
+            acc0[i] += wk[i] * x.x;
+            acc0[i + 1] += wk[i + 1] * x.y;
+            acc0[i + 2] += wk[i + 2] * x.z;
+            acc0[i + 3] += wk[i + 3] * x.w;
+            acc1[i] += wk[i] * y.x;
+            acc1[i + 1] += wk[i + 1] * y.y;
+            acc1[i + 2] += wk[i + 2] * y.z;
+            acc1[i + 3] += wk[i + 3] * y.w;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          stage[(16 * ch + i) * kD + tr] = __bfloat16_as_ushort(__float2bfloat16_rn(acc0[i]));
+          stage[(16 * ch + i) * kD + 128 + tr] = __bfloat16_as_ushort(__float2bfloat16_rn(acc1[i]));
+        }
+      }
+      if (xsync(false) < 0) break;
+      // copy out: 2048 16-byte granules (64 rows of 512 bytes), 16 per thread, row-contiguous
+      {
+        uint16_t* orow = p.out + t * p.out_st;
+#pragma unroll 4
+        for (int j = 0; j < 16; ++j) {
+          const int q = tr + 128 * j, h = q >> 5, gq = q & 31;
+          *reinterpret_cast<uint4*>(orow + (int64_t)h * p.out_sh + gq * 8) =
+              *reinterpret_cast<const uint4*>(stage + h * kD + gq * 8);
+        }
+      }
+      tc_fence_before();
+    }
+  } else if (warp >= 8) {
+    // ====================================================== row loaders (8 warps) ====
+    // Warp dw fills rows dw, dw + 8, ... of each K tile in the 128-byte-swizzled K-major layout
+    // (row r, 16-byte granule q of 64-column chunk c at c*128*128 + r*128 + ((q ^ (r&7)) << 4)).
+    // Rows past n_valid are zero (their keys are masked: a zero row keeps 0 * V finite).
+    const int dw = warp - 8;
+    uint32_t mc = 0, g = 0;
+    if constexpr (!C::FP8) {
+      while (!*abort_flag) {
+        const int st = mc % kMST;
+        if (!wait(m_full(st), (mc / kMST) & 1)) break;
+        const MetaHdr* mh = reinterpret_cast<const MetaHdr*>(smem + C::META_OFF + st * C::META_BYTES);
+        const int type = mh->type;
+        if (type != kTile) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(m_empty(st));
+          ++mc;
+          if (type == kDone) break;
+          continue;
+        }
+        const int n_valid = mh->n_valid;
+        const int* slots = reinterpret_cast<const int*>(reinterpret_cast<const uint8_t*>(mh) + 32);
+        const int ks = g % kKST;
+        uint8_t* kt = smem + C::KT_OFF + ks * C::KT_BYTES;
+        if (g >= (uint32_t)kKST && !wait(k_empty(ks), ((g / kKST) & 1) ^ 1)) break;
+        // one 512-byte row per warp-instruction: lane q copies granule q (chunk q/8, granule q%8)
+        const int ch = lane >> 3, gr = lane & 7;
+#pragma unroll 4
+        for (int k = 0; k < kRPW; ++k) {
+          const int r = dw + kNLD * k;
+          const bool v = r < n_valid;
+          const uint8_t* row = p.cache + (v ? (int64_t)slots[r] : 0) * (2 * kD);
+          const uint32_t dst = smem_u32(kt + ch * (kBN * 128) + r * 128 + ((gr ^ (r & 7)) << 4));
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(row + 16 * lane),
+                       "r"(v ? 16 : 0)
+                       : "memory");
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(m_empty(st));
+        ++mc;
+        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(k_full(ks)) : "memory");
+        ++g;
+      }
+    } else {
+      // Packed rows, two tiles in flight per warp: the loads of the next tile are issued before
+      // the current one is widened and stored. Lane l holds codes 8l .. 8l+7 of each of its
+      // rows; lanes 0-15 hold the two tile scales of row dw + 8 * lane.
+      struct Rows {
+        uint2 c[kRPW];
+        float2 sc;
+        int n_valid;
+      };
+      // fetch() waits for the next tile's slot list (skipping segment ends), issues its loads and
+      // releases the meta entry. It returns 1 when a tile was fetched, 0 at the end of the
+      // stream, and -1 (only when `block` is false) when the next entry is not published yet.
+      auto fetch = [&](Rows& R, bool block) -> int {
+        while (!*abort_flag) {
+          const int st = mc % kMST;
+          if (!block && !mbar_test(m_full(st), (mc / kMST) & 1)) return -1;
+          if (!wait(m_full(st), (mc / kMST) & 1)) return 0;
+          const MetaHdr* mh = reinterpret_cast<const MetaHdr*>(smem + C::META_OFF + st * C::META_BYTES);
+          const int type = mh->type;
+          if (type == kTile) {
+            const int n = mh->n_valid;
+            R.n_valid = n;
+            const int* slots = reinterpret_cast<const int*>(reinterpret_cast<const uint8_t*>(mh) + 32);
+#pragma unroll
+            for (int k = 0; k < kRPW; ++k) {
+              const int r = dw + kNLD * k;
+              if (r < n) R.c[k] = __ldg(reinterpret_cast<const uint2*>(p.cache + (int64_t)slots[r] * C::RB + 8 * lane));
+            }
+            const int rs = dw + kNLD * lane;
+            R.sc = (lane < kRPW && rs < n)
+                       ? __ldg(reinterpret_cast<const float2*>(p.cache + (int64_t)slots[rs] * C::RB + kD))
+                       : make_float2(0.0f, 0.0f);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(m_empty(st));
+          ++mc;
+          if (type == kTile) return 1;
+          if (type == kDone) return 0;
+        }
+        return 0;
+      };
+      // widen the rows of R into the next K stage (and their scales), then publish it
+      auto convert = [&](const Rows& R) -> bool {
+        const int ks = g % kKST;
+        uint8_t* kt = smem + C::KT_OFF + ks * C::KT_BYTES;
+        if (g >= (uint32_t)kKST && !wait(k_empty(ks), ((g / kKST) & 1) ^ 1)) return false;
+        const int ch = lane >> 3, gr = lane & 7;
+#pragma unroll
+        for (int k = 0; k < kRPW; ++k) {
+          const int r = dw + kNLD * k;
+          uint4 o = make_uint4(0, 0, 0, 0);
+          if (r < R.n_valid) {
+            o.x = e4m3x2_to_bf16x2_exact<0x9180u>(R.c[k].x);
+            o.y = e4m3x2_to_bf16x2_exact<0xB3A2u>(R.c[k].x);
+            o.z = e4m3x2_to_bf16x2_exact<0x9180u>(R.c[k].y);
+            o.w = e4m3x2_to_bf16x2_exact<0xB3A2u>(R.c[k].y);
+          }
+          *reinterpret_cast<uint4*>(kt + ch * (kBN * 128) + r * 128 + ((gr ^ (r & 7)) << 4)) = o;
+        }
+        if (lane < kRPW)
+          *reinterpret_cast<float2*>(smem + C::SC_OFF + ks * C::SC_BYTES + (dw + kNLD * lane) * 8) = R.sc;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(k_full(ks));
+        ++g;
+        return true;
+      };
+      // The next tile is fetched ahead only when its entry is already published: waiting for it
+      // before storing the current tile could deadlock at a segment boundary (the next segment's
+      // first entry waits for its Q buffer, i.e. for this tile's score product). One fetch and
+      // one convert site: ra holds the fetched, not yet stored tile (when have_a), rb the next.
+      Rows ra, rb;
+      bool have_a = false;
+      for (;;) {
+        const int r = fetch(rb, !have_a);  // block only when there is nothing to store meanwhile
+        if (have_a) {
+          if (!convert(ra)) break;
+          have_a = false;
+        }
+        if (r == 1) {
+          ra = rb;
+          have_a = true;
+        } else if (r == 0) {
+          break;
+        }
+      }
+    }
+    // drain this thread's outstanding cp.async copies before the CTA can finish
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int KIND>
+static dsa_status_t launch(const dsa_attn_args_t* a, const DeviceInfo& dev, cudaStream_t stream) {
+  using C = Cfg<KIND>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(attn_k128_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  });
+  if (attr_err != cudaSuccess) return cuda_fail(attr_err);
+  CUtensorMap tq;
+  dsa_status_t st = encode_q_tensor_map(a, kD, &tq);
+  if (st != DSA_OK) return st;
+
+  Params p{};
+  p.cache = static_cast<const uint8_t*>(a->cache);
+  p.num_slots = a->num_slots;
+  p.idx = a->indices;
+  p.idx_stride = a->idx_stride_t;
+  p.topk = a->topk;
+  p.bt = a->block_table;
+  p.bt_stride = a->bt_stride;
+  p.page_size = a->block_table ? a->page_size : 1;
+  p.max_pages = a->block_table ? a->max_pages : 0;
+  {
+    // round-up reciprocal: with l = ceil(log2 d) and m = ceil(2^(31+l) / d) < 2^32,
+    // floor(x * m / 2^(31+l)) == floor(x / d) for every 0 <= x < 2^31
+    const uint64_t d = (uint64_t)p.page_size;
+    int l = 0;
+    while ((1ull << l) < d) ++l;
+    p.pg_mul = (uint32_t)(((1ull << (31 + l)) + d - 1) / d);
+    p.pg_shift = 31 + l;
+  }
+  p.req = a->req_of_token;
+  p.c_log2 = a->sm_scale * 1.4426950408889634f;
+  p.out = static_cast<uint16_t*>(a->out);
+  p.out_st = a->out_stride_t;
+  p.out_sh = a->out_stride_h;
+  p.lse = a->lse;
+  const AttnWorkspace ws = attn_ws_layout(a->workspace, dev.sm_count);
+  p.ws_o = ws.o;
+  p.ws_ml = ws.ml;
+  p.flags = ws.flags;
+  p.err = a->error_word;
+  p.epoch = next_attn_epoch(a->workspace);
+  p.T = a->T;
+  p.NT = (a->topk + kBN - 1) / kBN;
+  p.U = a->T * (int64_t)p.NT;
+  // one persistent CTA per SM, with at least 4 units per CTA (small batches split each token
+  // into few parts), and few enough CTAs that a token spans at most kMaxParts + 1 of them
+  int64_t G = (p.U + 3) / 4;
+  if (G > dev.sm_count) G = dev.sm_count;
+  while (G > 1) {
+    const int64_t upc = p.U / G;  // fewest units any CTA holds
+    if ((p.NT + upc - 1) / upc + 1 <= kMaxParts + 1) break;
+    --G;
+  }
+  p.G = (int)G;
+
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)p.G);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_k128_kernel<KIND>, p, tq);
+  return e == cudaSuccess ? DSA_OK : cuda_fail(e);
+}
+
+}  // namespace k128
+
+dsa_status_t launch_attn_k128(const dsa_attn_args_t* a, const DeviceInfo& dev, cudaStream_t stream) {
+  if (a->kind == DSA_CACHE_BF16) return k128::launch<DSA_CACHE_BF16>(a, dev, stream);
+  return k128::launch<DSA_CACHE_FP8_SCALED>(a, dev, stream);
+}
+
+}  // namespace dsa

@@ -57,13 +57,18 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // Bounded wait: polls until the phase with the given parity has completed, or gives up once
 // `limit_ns` of wall time (the GPU's global timer) has passed. Returns false on timeout; the
 // caller records DSA_DEVERR_TIMEOUT and stops issuing work.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = 2000000000ull) {
-  if (mbar_try_wait(bar, parity)) return true;
+// The retry loop is out of line: every wait site costs one try and a call in the instruction
+// stream, not a copy of the loop.
+static __device__ __noinline__ bool mbar_wait_retry(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = 2000000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_retry(bar, parity, limit_ns);
 }
 
 // ------------------------------------------------------------------------- async copies --
@@ -156,6 +161,20 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// The same MMA with each descriptor given as its (low, high) 32-bit words and a compile-time
+// accumulate flag. Operand offsets then cost one 32-bit add on the low word (the address field
+// never carries into the high word for shared-memory operands below 256 KB), which keeps a
+// single issuing thread ahead of the tensor core.
+template <int ACC>
+__device__ __forceinline__ void mma_bf16_lohi(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                              uint32_t b_hi, uint32_t idesc) {
+  asm volatile(
+      "{\n.reg .b64 da, db;\n.reg .pred p;\nmov.b64 da, {%1, %2};\nmov.b64 db, {%3, %4};\n"
+      "setp.ne.b32 p, %6, 0;\ntcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "n"(ACC)
+      : "memory");
+}
+
 // Arrive (once) on an mbarrier when all previously issued tcgen05 MMAs of this thread complete.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -201,6 +220,39 @@ __device__ __forceinline__ void tmem_st16x2_x32(uint32_t taddr, const uint32_t (
       : "memory");
 }
 
+// 32 lanes x 32 bit: thread i of the warp reads / writes TMEM lane (warp's quarter base + i),
+// columns c, c+1, ... (one 32-bit column per register).
+__device__ __forceinline__ void tmem_ld32_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// Warp-wide maximum of a signed integer.
+__device__ __forceinline__ int redux_max_s32(int v) {
+  int r;
+  asm volatile("redux.sync.max.s32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+  return r;
+}
+
+// Order-preserving map between finite / infinite floats and signed integers (an involution):
+// a < b as floats iff f2ord(a) < f2ord(b) as signed integers.
+__device__ __forceinline__ int f2ord(float f) {
+  const int b = __float_as_int(f);
+  return b ^ ((b >> 31) & 0x7FFFFFFF);
+}
+__device__ __forceinline__ float ord2f(int k) { return __int_as_float(k ^ ((k >> 31) & 0x7FFFFFFF)); }
+
 // 2^x on the MUFU unit (flushes subnormal results to zero; exp2(-inf) = 0).
 __device__ __forceinline__ float ex2_approx(float x) {
   float r;
@@ -228,6 +280,22 @@ __device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t h2) {
 __device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Exact widening of two e4m3 codes to bf16 without a scale. `sel` picks the two source bytes of
+// `w` with the sign of each replicated into the byte above it (0x9180: bytes 0, 1; 0xB3A2:
+// bytes 2, 3). Shifting sign-extended 16-bit halves left by 4 and keeping bits 0x87F0 puts the
+// code's sign at bf16 bit 15 and its 4-bit exponent and 3-bit mantissa at bits 10..4, i.e. a
+// bf16 with the code's value times 2^-120 (e4m3 subnormals land on bf16 subnormals); the
+// multiply by 2^120 (bf16 0x7B80) is exact. Codes 0x7F / 0xFF (NaN in e4m3) are never written
+// by the packer and would read as +-480.
+template <uint32_t SEL>
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_exact(uint32_t w) {
+  uint32_t t, r;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(t) : "r"(w), "n"(SEL));
+  t = (t << 4) & 0x87F087F0u;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(0x7B807B80u));
   return r;
 }
 

@@ -117,6 +117,30 @@ class NormalRows:
 
 
 @dataclass
+class FixedRows:
+    """Explicit bf16 rows (uint16 bits [rows, cols]) with the interface of NormalRows."""
+
+    data: np.ndarray
+
+    @property
+    def rows(self) -> int:
+        return int(self.data.shape[0])
+
+    @property
+    def cols(self) -> int:
+        return int(self.data.shape[1])
+
+    def bits(self, row_ids=None) -> np.ndarray:
+        if row_ids is None:
+            return self.data
+        return self.data[np.asarray(row_ids, dtype=np.int64).ravel()]
+
+    def torch(self, device):
+        import torch
+        return torch.from_numpy(np.ascontiguousarray(self.data).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+@dataclass
 class Workload:
     """One synthetic sparse-attention problem.
 
@@ -131,10 +155,10 @@ class Workload:
     d_nope: int
     d_rope: int
     d_v: int
-    q: NormalRows                      # [T*H, D] rows of the query (reshaped to [T, H, D])
+    q: "NormalRows | FixedRows"        # [T*H, D] rows of the query (reshaped to [T, H, D])
     T: int
     H: int
-    kv: NormalRows                     # [num_slots, D] latent rows (slot order)
+    kv: "NormalRows | FixedRows"       # [num_slots, D] latent rows (slot order)
     num_slots: int
     indices: np.ndarray                # int32 [T, topk]
     sm_scale: float

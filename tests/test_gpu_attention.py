@@ -45,32 +45,28 @@ def _check(wl, device, tokens=None, lse=True):
     """Output and LSE against the oracle.
 
     BF16 cache: the oracle sees exactly the kernel's inputs (fp32 accumulation is the only
-    difference; LSE within 2e-4). FP8 cache: the reference is the fp64 oracle over the same
-    dequantised rows the kernel computes on (bf16_rne(code * scale), the gather/dequant helper's
-    output), checked to the same tolerances; in addition, where the scores are of order one
-    (sm_scale <= 1/sqrt(D), the regime of the named workloads), the output is also checked
-    against the oracle's exact dequantisation (code * scale in fp64), with the LSE bound that
-    follows from the bf16 rounding of the keys: |ds| <= sm_scale * 2^-9 * sum_d |q_d k_d|, at
-    most about 2e-2 for unit-variance rows of width 256."""
+    difference; LSE within 2e-4). FP8 cache: the kernel never rounds a dequantised value; it
+    multiplies the exact e4m3 codes and applies each row's fp32 tile scales to its score
+    accumulators and to the probabilities, so the reference is the oracle's exact dequantisation
+    (code * scale in fp64), to the same tolerances as BF16. Where the scores are of order one
+    (sm_scale <= 1/sqrt(D), the regime of the named workloads) the output is also checked
+    against the oracle over the bf16-rounded rows of the gather/dequant helper, with the LSE
+    bound that follows from that rounding: |ds| <= sm_scale * 2^-9 * sum_d |q_d k_d|, at most
+    about 2e-2 for unit-variance rows of width 256."""
     cache = oracle_cache(wl)
     out, lse_t = _gpu_attn(wl, cache, device, lse=lse)
     got = f32_of(out) if tokens is None else f32_of(out)[tokens]
     g_lse = None if not lse else (f32_of(lse_t) if tokens is None else f32_of(lse_t)[tokens])
     ref, ref_lse, bad = run_oracle(wl, cache, tokens=tokens)
     assert bad == 0
-    if wl.kind == 0:
-        check_close(got, ref, wl.name)
-        if lse:
-            _check_lse(g_lse, ref_lse, 2e-4)
-        return out
-    ref_d, ref_lse_d, _ = run_oracle_on_dequantised(wl, cache, tokens=tokens)
-    check_close(got, ref_d, wl.name + " (dequantised rows)")
+    check_close(got, ref, wl.name + (" (exact dequantisation)" if wl.kind == 1 else ""))
     if lse:
-        _check_lse(g_lse, ref_lse_d, 2e-4)
-    if wl.sm_scale <= 1.0 / np.sqrt(wl.D) + 1e-12:
-        check_close(got, ref, wl.name + " (exact dequantisation)")
+        _check_lse(g_lse, ref_lse, 2e-4)
+    if wl.kind == 1 and wl.sm_scale <= 1.0 / np.sqrt(wl.D) + 1e-12:
+        ref_d, ref_lse_d, _ = run_oracle_on_dequantised(wl, cache, tokens=tokens)
+        check_close(got, ref_d, wl.name + " (bf16-rounded dequantised rows)")
         if lse:
-            _check_lse(g_lse, ref_lse, 2e-2)
+            _check_lse(g_lse, ref_lse_d, 2e-2)
     return out
 
 
@@ -225,15 +221,28 @@ def test_bit_identical_repeats(gpu):
             assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
 
 
-def test_fp8_attention_equals_bf16_attention_on_dequantised_rows(gpu):
-    """The FP8 path dequantises rows as bf16(code * scale): attention over the FP8 cache is
-    bit-identical to attention over a BF16 cache holding the gather/dequant helper's rows."""
-    wl = W.fp8_paged(T=8, requests=1, positions=4096, page_size=64, topk=2112, n_valid=2051, seed=15, sm_scale=1 / 16)
+def _scaled_halves(bits, lo, hi):
+    """bf16 bits with columns 0-127 multiplied by 2^lo and 128-255 by 2^hi (exact)."""
+    f = (bits.astype(np.uint32) << 16).view(np.float32).copy()
+    f[:, :128] *= 2.0 ** lo
+    f[:, 128:] *= 2.0 ** hi
+    return (f.view(np.uint32) >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("e", [10, -10])
+def test_fp8_tile_scales_applied_per_tile(gpu, e):
+    """Rows whose two 128-column tiles differ in magnitude by 2^20, so that their tile scales do,
+    with the query scaled inversely (scores stay of order one): the kernel applies each tile's
+    fp32 scale to its own half of the score and of the output. Each output half is compared
+    after undoing its exact power-of-two factor, i.e. at the precision of the unscaled problem;
+    the LSE is unaffected by the value scaling and is checked as is."""
+    wl = W.fp8_paged(T=6, requests=1, positions=4096, page_size=64, topk=2112, n_valid=2051, seed=15, sm_scale=1 / 16)
+    wl.kv = W.FixedRows(_scaled_halves(wl.kv.bits(), -e, e))
+    wl.q = W.FixedRows(_scaled_halves(wl.q.bits(), e, -e))
     cache = oracle_cache(wl)
-    out8, _ = _gpu_attn(wl, cache, gpu)
-    deq, _ = oracle.gather_dequant(cache, 1, 256, 0, np.arange(wl.num_slots, dtype=np.int32))
-    wl16 = W.fp8_paged(T=8, requests=1, positions=4096, page_size=64, topk=2112, n_valid=2051, seed=15,
-                       sm_scale=1 / 16)
-    wl16.kind = 0
-    out16, _ = _gpu_attn(wl16, deq, gpu)
-    assert torch.equal(out8.view(torch.int16), out16.view(torch.int16))
+    out, lse_t = _gpu_attn(wl, cache, gpu, lse=True)
+    ref, ref_lse, bad = run_oracle(wl, cache)
+    assert bad == 0
+    undo = np.concatenate([np.full(128, 2.0 ** e), np.full(128, 2.0 ** -e)])
+    check_close(f32_of(out) * undo, ref * undo, "fp8 tile scales")
+    _check_lse(f32_of(lse_t), ref_lse, 2e-4)
