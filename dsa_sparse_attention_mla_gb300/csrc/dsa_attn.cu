@@ -954,10 +954,10 @@ dsa_status_t encode_q_tensor_map(const dsa_attn_args_t* a, int dk, CUtensorMap* 
 }
 
 size_t attn_ws_bytes(int sm_count) {
-  // partial o [G][64][256] fp32 + (max, sum) [G][2][64] fp32 + flags [G][4] int32
+  // partial o [G][64][256] fp32 + (max, sum) [G][2][64] fp32 + flags [G][8] int32
   const size_t o = (size_t)sm_count * kHeads * 256 * 4;
   const size_t ml = (size_t)sm_count * 2 * kHeads * 4;
-  const size_t fl = ((size_t)sm_count * 16 + 255) & ~size_t(255);
+  const size_t fl = ((size_t)sm_count * 32 + 255) & ~size_t(255);
   return o + ml + fl;
 }
 
@@ -1109,7 +1109,7 @@ dsa_status_t dsa_sparse_attn(const dsa_attn_args_t* a, void* stream) {
 namespace dsa {
 constexpr int kStaticWsCtas = 160;
 constexpr size_t kStaticWsBytes = (size_t)kStaticWsCtas * kHeads * 256 * 4 + (size_t)kStaticWsCtas * 2 * kHeads * 4 +
-                                  (((size_t)kStaticWsCtas * 16 + 255) & ~size_t(255));
+                                  (((size_t)kStaticWsCtas * 32 + 255) & ~size_t(255));
 static __device__ __align__(256) uint8_t g_static_ws[kStaticWsBytes];
 
 // Device address of g_static_ws for the current device, looked up once per device (the host

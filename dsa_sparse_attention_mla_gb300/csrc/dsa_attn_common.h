@@ -20,7 +20,7 @@ dsa_status_t encode_q_tensor_map(const dsa_attn_args_t* a, int dk, CUtensorMap* 
 int next_attn_epoch(const void* workspace);
 
 // Workspace of the split-token merge, per persistent CTA b: partial o [b][64 * 256] fp32,
-// (max, sum) [b][2][64] fp32 and four publish flags [b][4] int32.
+// (max, sum) [b][2][64] fp32 and eight publish flags [b][8] int32.
 size_t attn_ws_bytes(int sm_count);
 struct AttnWorkspace {
   float* o;

@@ -36,6 +36,7 @@
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "dsa_attn_common.h"
 #include "dsa_host.h"
@@ -49,11 +50,16 @@ constexpr int kD = 256;         // latent width (= d_v)
 constexpr int kBN = 128;        // gathered keys per tile: MMA M
 constexpr int kKST = 2;         // K tile stages
 constexpr int kMST = 8;         // meta ring depth
-constexpr int kNLD = 8;         // loader warps
-constexpr int kWarps = 8 + kNLD;
+constexpr int kNSM = 4;         // softmax warps (4-7): one per TMEM lane quarter
+constexpr int kHW = kH * 4 / kNSM;  // heads per softmax warp
+constexpr int kCH = kHW / 16;       // 16-head chunks per softmax warp
+constexpr int kNLD = 9;         // loader warps: 3 and 8-15
+constexpr int kWarps = 16;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kRPW = kBN / kNLD;  // rows per loader warp per tile
-constexpr int kMaxParts = 32;     // most parts of one split token (the launch guarantees it)
+// loader warp index (3 -> 0, 8..15 -> 1..8), -1 for other warps
+__device__ __forceinline__ int loader_index(int warp) { return warp == 3 ? 0 : (warp >= 8 ? warp - 7 : -1); }
+constexpr int kMaxParts = 16;     // most parts of one split token (the launch guarantees it)
+constexpr int kRing = 8;          // packed rows in flight per loader warp (shared-memory ring)
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 template <int KIND>
@@ -74,9 +80,11 @@ struct Cfg {
   static constexpr int META_OFF = SC_OFF + kKST * SC_BYTES;
   static constexpr int META_BYTES = 32 + 4 * kBN;
   static constexpr int CMP_OFF = META_OFF + kMST * META_BYTES;  // producer: one step's valid slots
-  static constexpr int RED_OFF = CMP_OFF + 4 * 256;
-  // m[64], alpha[64], lsum[64], spare[64], part[4][64], wk[kMaxParts][64], votes[2][4]
-  static constexpr int RED_FLOATS = 8 * kH + kMaxParts * kH + 8;
+  static constexpr int RING_OFF = CMP_OFF + 4 * 256;                // packed-row loaders: code rings
+  static constexpr int RING_BYTES = FP8 ? kNLD * kRing * 256 : 0;
+  static constexpr int RED_OFF = RING_OFF + RING_BYTES;
+  // m[64], alpha[64], lsum[64], spare[64], part[4][64], wk[kMaxParts][64], votes[2][8]
+  static constexpr int RED_FLOATS = 8 * kH + kMaxParts * kH + 2 * kNSM;
   static constexpr int BAR_OFF = RED_OFF + ((RED_FLOATS * 4 + 15) & ~15);
   static constexpr int NBARS = 2 + 2 * kKST + 2 * kMST + 8 + 3;
   static constexpr int MISC_OFF = BAR_OFF + 8 * NBARS;
@@ -84,9 +92,9 @@ struct Cfg {
   // tensor memory columns
   static constexpr int S_COLS = 64 * NSUB;  // per S buffer (two buffers)
   static constexpr int O_COL = 2 * S_COLS;  // O^T halves: dv 0-127 at O_COL, dv 128-255 at O_COL + 64
-  static constexpr int L_COL = O_COL + 128;
+  static constexpr int L_COL = O_COL + 128;  // per-lane partial row sums, two buffers of 64 columns
   static constexpr int TMEM_COLS = 512;
-  static_assert(L_COL + 64 <= TMEM_COLS, "TMEM budget");
+  static_assert(L_COL + 128 <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(KT_OFF % 1024 == 0 && P_OFF % 1024 == 0 && KT_BYTES % 1024 == 0, "operand alignment");
 };
@@ -125,7 +133,7 @@ struct Params {
   float* lse;
   float* ws_o;   // [G][256 dv][64 heads] partial O^T (unnormalised, relative to its max)
   float* ws_ml;  // [G][2][64] partial max (exp2 domain) and row sum
-  int* flags;    // [G][4] partial published (holds the call's epoch), one per softmax warp
+  int* flags;    // [G][8] partial published (holds the call's epoch), one per softmax warp
   int epoch;
   int32_t* err;
   int64_t T;
@@ -141,19 +149,22 @@ __device__ __forceinline__ int64_t unit_begin(int64_t b, int64_t U, int G) { ret
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 __device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
 
-// Exchange among the four softmax warps (one arrival each on `xbar`, phase `n` of it): returns
-// the OR of `v` over the warps, with every warp's earlier shared-memory writes visible, or -1
-// when a warp did not arrive within the time limit.
-static __device__ __noinline__ int softmax_exchange(uint32_t xbar, int* votes, uint32_t n, int sp, int v) {
+// Exchange among the softmax warps (one arrival each on `xbar`, phase `n` of it; `sm` is the
+// warp's softmax index): returns the OR of `v` over the warps, with every warp's earlier
+// shared-memory writes visible, or -1 when a warp did not arrive within the time limit.
+static __device__ __noinline__ int softmax_exchange(uint32_t xbar, int* votes, uint32_t n, int sm, int v) {
   const int lane = threadIdx.x & 31;
   const int slot = n & 1;
   const bool any = __any_sync(0xffffffffu, v != 0);
-  if (lane == 0) votes[slot * 4 + sp] = any ? 1 : 0;
+  if (lane == 0) votes[slot * kNSM + sm] = any ? 1 : 0;
   __syncwarp();
   if (lane == 0) mbar_arrive(xbar);
   const bool ok = mbar_wait(xbar, n & 1, kWaitNs);
   if (!__all_sync(0xffffffffu, ok)) return -1;
-  return (votes[slot * 4] | votes[slot * 4 + 1] | votes[slot * 4 + 2] | votes[slot * 4 + 3]) ? 1 : 0;
+  int r = 0;
+#pragma unroll
+  for (int w = 0; w < kNSM; ++w) r |= votes[slot * kNSM + w];
+  return r ? 1 : 0;
 }
 
 template <int KIND>
@@ -176,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto s_empty = [&](int i) { return x0 + 16 + 8 * i; };
   auto p_full = [&](int i) { return x0 + 32 + 8 * i; };
   auto pv_done = [&](int i) { return x0 + 48 + 8 * i; };
-  const uint32_t xbar = x0 + 64;        // softmax-warp exchange (4 arrivals per phase)
+  const uint32_t xbar = x0 + 64;        // softmax-warp exchange (one arrival per softmax warp)
   const uint32_t mma_drain = x0 + 72;   // every MMA of an issuer complete (x0 + 72: scores, + 80: output)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
@@ -191,15 +202,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < kMST; ++s) {
       mbar_init(m_full(s), 1);
-      mbar_init(m_empty(s), 2 + 4 + kNLD);  // 2 MMA threads, 4 softmax, loader warps
+      mbar_init(m_empty(s), 2 + kNSM + kNLD);  // 2 MMA threads, softmax warps, loader warps
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(s_full(i), 1);
-      mbar_init(s_empty(i), 4);
-      mbar_init(p_full(i), 4);
+      mbar_init(s_empty(i), kNSM);
+      mbar_init(p_full(i), kNSM);
       mbar_init(pv_done(i), 1);
     }
-    mbar_init(xbar, 4);
+    mbar_init(xbar, kNSM);
     mbar_init(mma_drain, 1);
     mbar_init(mma_drain + 8, 1);
     *abort_flag = 0;
@@ -487,20 +498,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(drain, 0, kWaitNs);
     }
     __syncwarp();
-  } else if (warp >= 4 && warp < 8) {
-    // =============================================== softmax + epilogue (4 warps) ====
-    const int sp = warp & 3;                                 // TMEM lane quarter
-    const int tr = 32 * sp + lane;                           // key row of the tile / dv row of O^T
-    const uint32_t tl = tmem + ((uint32_t)(32 * sp) << 16);  // this warp's lanes
+  } else if (warp >= 4 && warp < 4 + kNSM) {  // (softmax)
+    // ============================================== softmax + epilogue (8 warps) ====
+    // Thread = key of the tile = TMEM lane (quarter warp % 4); the two warps of a quarter take
+    // heads 0-31 and 32-63. Per tile one pass computes, with the running max m_h of each head,
+    // x = c * score - m_h, p = 2^x, the per-lane partial row sums (TMEM, two buffers: the pass
+    // reads one and writes the other) and the probability rows of P. A vote of the eight warps
+    // then checks that no x exceeded 8; if one did (rare after a segment's first tile), the
+    // tile takes exact per-head maxima, raises m_h where it grew by more than 2^8, rescales O
+    // and the partial sums of those heads, and is redone. A segment's first tile starts there.
+    const int sm = warp - 4;                                 // softmax warp index
+    const int qd = warp & 3;                                 // TMEM lane quarter
+    const int hb = kHW * (sm >> 2);                          // first head of this warp
+    const int tr = 32 * qd + lane;                           // key row of the tile / dv row of O^T
+    const int sid = 32 * sm + lane;                          // softmax thread index
+    const uint32_t tl = tmem + ((uint32_t)(32 * qd) << 16);  // this warp's lanes
     float* red = reinterpret_cast<float*>(smem + C::RED_OFF);
     float* red_m = red;           // running max per head (exp2 domain)
     float* red_alpha = red + 64;  // rescale factor per head; epilogue: weight of own partial
-    float* red_part = red + 256;  // [4 warps][64 heads]
+    float* red_l = red + 128;     // epilogue: row sum per head
+    float* red_part = red + 256;  // [4 lane quarters][64 heads]
     float* red_wk = red + 512;    // [kMaxParts][64]: merge weights of the other parts
-    int* votes = reinterpret_cast<int*>(red + 512 + kMaxParts * kH);  // [2][4]
-    uint32_t mc = 0, g = 0, xc = 0;
+    int* votes = reinterpret_cast<int*>(red + 512 + kMaxParts * kH);  // [2][kNSM]
+    uint32_t mc = 0, g = 0, xc = 0, lb = 0;
     auto xsync = [&](bool v) -> int {
-      const int r = softmax_exchange(xbar, votes, xc++, sp, v ? 1 : 0);
+      const int r = softmax_exchange(xbar, votes, xc++, sm, v ? 1 : 0);
       if (r < 0) fail(DSA_DEVERR_TIMEOUT);
       return r;
     };
@@ -508,6 +530,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (__all_sync(0xffffffffu, ok)) return true;
       fail(DSA_DEVERR_TIMEOUT);
       return false;
+    };
+    // every PV product up to tile `last` (inclusive) complete
+    auto pv_wait = [&](int64_t last) -> bool {
+      if (last < 0) return true;
+      return mbar_wait(pv_done((uint32_t)last & 1), ((uint32_t)last >> 1) & 1, kWaitNs);
     };
     for (;;) {
       const int st = mc % kMST;
@@ -529,6 +556,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = mbar_wait(s_full(g & 1), (g >> 1) & 1, kWaitNs);
         // the tile scales come from the loaders: acquire their stage barrier directly
         if constexpr (C::FP8) ok = ok && mbar_wait(k_full(ks), (g / kKST) & 1, kWaitNs);
+        // the P buffer must be free: the PV product that read it last is complete
+        ok = ok && pv_wait((int64_t)g - C::PBUF);
         if (!wait_all(ok)) break;
         tc_fence_after();
         const bool valid = tr < n_valid;
@@ -539,120 +568,113 @@ __global__ void __launch_bounds__(kThreads, 1)
           sc1 = sc.y;
         }
         const float c0 = p.c_log2 * sc0, c1 = p.c_log2 * sc1;
-        const uint32_t sa = tl + (g & 1) * C::S_COLS;
+        const uint32_t sa = tl + (g & 1) * C::S_COLS + hb;
+        const uint32_t lcur = tl + C::L_COL + 64 * lb + hb, lnxt = tl + C::L_COL + 64 * (lb ^ 1) + hb;
+        uint8_t* prow = smem + C::P_OFF + (g % C::PBUF) * C::P_BYTES + tr * 128;
+        const int sw = tr & 7;
         // score of head i of a chunk, exp2 domain, before subtracting the running max
         auto score = [&](const uint32_t (&a)[16], const uint32_t (&bb)[16], int i) -> float {
           if constexpr (C::FP8) return fmaf(u2f(a[i]), c0, u2f(bb[i]) * c1);
           else return u2f(a[i]) * c0;
         };
-        bool slow = first != 0;
-        if (!slow) {
-          // does any valid key exceed its head's running max by more than 2^8?
+        bool exact = first != 0, bad = false;
+        for (;;) {
+          bool resc = false;
+          if (exact) {
+            // exact per-head maximum of this tile: warp max-reductions over the keys, then
+            // across the four lane quarters
+#pragma unroll 1
+            for (int ch = 0; ch < kCH; ++ch) {
+              uint32_t a[16], bb[16];
+              tmem_ld32_x16(sa + 16 * ch, a);
+              if constexpr (C::FP8) tmem_ld32_x16(sa + 64 + 16 * ch, bb);
+              tc_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int mx = redux_max_s32(f2ord(valid ? score(a, bb, i) : -INFINITY));
+                if (lane == ((16 * ch + i) & 31)) red_part[qd * 64 + hb + 16 * ch + i] = ord2f(mx);
+              }
+            }
+            if (xsync(false) < 0) { bad = true; break; }
+            bool grow_any = false;
+            if (sid < kH) {
+              const float mt = fmaxf(fmaxf(red_part[sid], red_part[64 + sid]), fmaxf(red_part[128 + sid], red_part[192 + sid]));
+              const float mo = first ? -INFINITY : red_m[sid];
+              const bool grow = first || mt > mo + 8.0f;
+              const float mn = grow ? mt : mo;
+              red_alpha[sid] = grow ? ex2_approx(mo - mn) : 1.0f;
+              red_m[sid] = mn;
+              grow_any = grow && !first;
+            }
+            const int r = xsync(grow_any);
+            if (r < 0) { bad = true; break; }
+            resc = r != 0;
+          }
+          if (resc) {
+            // rare: some head's max grew; scale its O^T columns (every issued PV complete)
+            if (!wait_all(pv_wait((int64_t)g - 1))) { bad = true; break; }
+            tc_fence_after();
+#pragma unroll 1
+            for (int ch = 0; ch < kCH; ++ch) {
+              uint32_t o0[16], o1[16];
+              tmem_ld32_x16(tl + C::O_COL + hb + 16 * ch, o0);
+              tmem_ld32_x16(tl + C::O_COL + 64 + hb + 16 * ch, o1);
+              tc_wait_ld();
+              const float* al = red_alpha + hb + 16 * ch;
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                o0[i] = f2u(u2f(o0[i]) * al[i]);
+                o1[i] = f2u(u2f(o1[i]) * al[i]);
+              }
+              tmem_st32_x16(tl + C::O_COL + hb + 16 * ch, o0);
+              tmem_st32_x16(tl + C::O_COL + 64 + hb + 16 * ch, o1);
+            }
+          }
+          // the pass: p = 2^(c * score - m) (one FFMA and one MUFU ex2 per score), partial row
+          // sums into the other TMEM buffer (scaled by alpha after a rescale), and P (packed
+          // rows: p * scale of each tile) as bf16 into this key's 128-byte row
           float xm = -INFINITY;
 #pragma unroll 1
-          for (int ch = 0; ch < 4; ++ch) {
-            uint32_t a[16], bb[16];
+          for (int ch = 0; ch < kCH; ++ch) {
+            uint32_t a[16], bb[16], l[16];
             tmem_ld32_x16(sa + 16 * ch, a);
             if constexpr (C::FP8) tmem_ld32_x16(sa + 64 + 16 * ch, bb);
+            if (!first) tmem_ld32_x16(lcur + 16 * ch, l);
             tc_wait_ld();
-            const float* mrow = red_m + 16 * ch;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) xm = fmaxf(xm, score(a, bb, i) - mrow[i]);
-          }
-          const int r = xsync(valid && xm > 8.0f);
-          if (r < 0) break;
-          slow = r != 0;
-        }
-        bool resc = false;
-        if (slow) {
-          // exact per-head maximum of this tile: warp max-reductions, then across the 4 warps
-#pragma unroll 1
-          for (int ch = 0; ch < 4; ++ch) {
-            uint32_t a[16], bb[16];
-            tmem_ld32_x16(sa + 16 * ch, a);
-            if constexpr (C::FP8) tmem_ld32_x16(sa + 64 + 16 * ch, bb);
-            tc_wait_ld();
+            const float* mrow = red_m + hb + 16 * ch;
+            const float* al = red_alpha + hb + 16 * ch;
+            float pr[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const int mx = redux_max_s32(f2ord(valid ? score(a, bb, i) : -INFINITY));
-              if (lane == ((16 * ch + i) & 31)) red_part[sp * 64 + 16 * ch + i] = ord2f(mx);
+              const float x = score(a, bb, i) - mrow[i];
+              xm = fmaxf(xm, valid ? x : -INFINITY);
+              pr[i] = valid ? ex2_approx(x) : 0.0f;
+              float lv = pr[i];
+              if (!first) lv = exact ? fmaf(u2f(l[i]), al[i], pr[i]) : u2f(l[i]) + pr[i];
+              l[i] = f2u(lv);
+            }
+            tmem_st32_x16(lnxt + 16 * ch, l);
+            const int g0 = (hb >> 3) + 2 * ch;  // 16-byte granules of this chunk's 16 heads
+            uint32_t w[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) w[i] = f32x2_to_bf16x2(pr[2 * i] * sc0, pr[2 * i + 1] * sc0);
+            *reinterpret_cast<uint4*>(prow + ((g0 ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(prow + (((g0 + 1) ^ sw) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+            if constexpr (C::FP8) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) w[i] = f32x2_to_bf16x2(pr[2 * i] * sc1, pr[2 * i + 1] * sc1);
+              *reinterpret_cast<uint4*>(prow + kBN * 128 + ((g0 ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+              *reinterpret_cast<uint4*>(prow + kBN * 128 + (((g0 + 1) ^ sw) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
             }
           }
-          if (xsync(false) < 0) break;
-          bool grow_any = false;
-          if (tr < kH) {
-            const float mt =
-                fmaxf(fmaxf(red_part[tr], red_part[64 + tr]), fmaxf(red_part[128 + tr], red_part[192 + tr]));
-            const float mo = first ? -INFINITY : red_m[tr];
-            const bool grow = first || mt > mo + 8.0f;
-            const float mn = grow ? mt : mo;
-            red_alpha[tr] = grow ? ex2_approx(mo - mn) : 1.0f;
-            red_m[tr] = mn;
-            grow_any = grow && !first;
-          }
-          const int r = xsync(grow_any);
-          if (r < 0) break;
-          resc = r != 0;
+          if (exact) break;
+          const int r = xsync(xm > 8.0f);
+          if (r < 0) { bad = true; break; }
+          if (r == 0) break;
+          exact = true;
         }
-        // the P buffer must be free; a rescale also needs every issued PV complete
-        ok = true;
-        if (g >= (uint32_t)C::PBUF) ok = mbar_wait(pv_done((g - C::PBUF) & 1), ((g - C::PBUF) >> 1) & 1, kWaitNs);
-        if (resc && C::PBUF > 1 && g >= 1) ok = ok && mbar_wait(pv_done((g - 1) & 1), ((g - 1) >> 1) & 1, kWaitNs);
-        if (!wait_all(ok)) break;
-        tc_fence_after();
-        if (resc) {  // rare: some head's max grew; scale its O^T column and partial sums
-#pragma unroll 1
-          for (int ch = 0; ch < 4; ++ch) {
-            uint32_t o0[16], o1[16], l[16];
-            tmem_ld32_x16(tl + C::O_COL + 16 * ch, o0);
-            tmem_ld32_x16(tl + C::O_COL + 64 + 16 * ch, o1);
-            tmem_ld32_x16(tl + C::L_COL + 16 * ch, l);
-            tc_wait_ld();
-            const float* al = red_alpha + 16 * ch;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float a = al[i];
-              o0[i] = f2u(u2f(o0[i]) * a);
-              o1[i] = f2u(u2f(o1[i]) * a);
-              l[i] = f2u(u2f(l[i]) * a);
-            }
-            tmem_st32_x16(tl + C::O_COL + 16 * ch, o0);
-            tmem_st32_x16(tl + C::O_COL + 64 + 16 * ch, o1);
-            tmem_st32_x16(tl + C::L_COL + 16 * ch, l);
-          }
-        }
-        // probabilities: one FFMA and one MUFU ex2 per score; row sums into TMEM; P (or, for
-        // packed rows, p * scale of each tile) as bf16 into this key's 128-byte row
-        uint8_t* prow = smem + C::P_OFF + (g % C::PBUF) * C::P_BYTES + tr * 128;
-        const int sw = tr & 7;
-#pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t a[16], bb[16], l[16];
-          tmem_ld32_x16(sa + 16 * ch, a);
-          if constexpr (C::FP8) tmem_ld32_x16(sa + 64 + 16 * ch, bb);
-          tmem_ld32_x16(tl + C::L_COL + 16 * ch, l);
-          tc_wait_ld();
-          const float* mrow = red_m + 16 * ch;
-          float pr[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            pr[i] = valid ? ex2_approx(score(a, bb, i) - mrow[i]) : 0.0f;
-            l[i] = f2u(first ? pr[i] : u2f(l[i]) + pr[i]);
-          }
-          tmem_st32_x16(tl + C::L_COL + 16 * ch, l);
-          uint32_t w[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) w[i] = f32x2_to_bf16x2(pr[2 * i] * sc0, pr[2 * i + 1] * sc0);
-          *reinterpret_cast<uint4*>(prow + (((2 * ch) ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-          *reinterpret_cast<uint4*>(prow + (((2 * ch + 1) ^ sw) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
-          if constexpr (C::FP8) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) w[i] = f32x2_to_bf16x2(pr[2 * i] * sc1, pr[2 * i + 1] * sc1);
-            *reinterpret_cast<uint4*>(prow + kBN * 128 + (((2 * ch) ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-            *reinterpret_cast<uint4*>(prow + kBN * 128 + (((2 * ch + 1) ^ sw) << 4)) =
-                make_uint4(w[4], w[5], w[6], w[7]);
-          }
-        }
+        if (bad) break;
+        lb ^= 1;
         fence_proxy_async_smem();
         tc_wait_st();
         tc_fence_before();
@@ -671,58 +693,57 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(m_empty(st));
       ++mc;
       if (had) {
-        if (!wait_all(mbar_wait(pv_done((g - 1) & 1), ((g - 1) >> 1) & 1, kWaitNs))) break;
+        if (!wait_all(pv_wait((int64_t)g - 1))) break;
         tc_fence_after();
       }
-      // row sums: each lane's 64 partial sums go to its row of a [128][64] fp32 block in the (idle)
-      // P buffers, 16-byte granule q of row r at ((q ^ (r & 15)) << 4); then thread h < 64 adds up
-      // column h (conflict-free: a warp reads 32 consecutive columns of one row)
+      const uint32_t lfin = tl + C::L_COL + 64 * lb + hb;  // the buffer the last pass wrote
+      // row sums: each lane's partial sums of its 32 heads go to its row of a [128][64] fp32
+      // block in the (idle) P buffers, 16-byte granule q of row r at ((q ^ (r & 15)) << 4); then
+      // thread h < 64 adds up column h (a warp reads 32 consecutive columns of one row)
       float* lrow = reinterpret_cast<float*>(smem + C::P_OFF);
-      {
-        float* dst = lrow + tr * kH;
 #pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t l[16];
-          if (had) {
-            tmem_ld32_x16(tl + C::L_COL + 16 * ch, l);
-            tc_wait_ld();
-          } else {
+      for (int ch = 0; ch < kCH; ++ch) {
+        uint32_t l[16];
+        if (had) {
+          tmem_ld32_x16(lfin + 16 * ch, l);
+          tc_wait_ld();
+        } else {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) l[i] = 0u;
-          }
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4*>(dst + ((((4 * ch + q) ^ (tr & 15))) << 2)) =
-                make_uint4(l[4 * q], l[4 * q + 1], l[4 * q + 2], l[4 * q + 3]);
+          for (int i = 0; i < 16; ++i) l[i] = 0u;
         }
-      }
-      if (xsync(false) < 0) break;
-      if (tr < kH) {
-        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll 4
-        for (int r = 0; r < kBN; ++r) acc[r & 3] += lrow[r * kH + ((((tr >> 2) ^ (r & 15))) << 2) + (tr & 3)];
-        red_part[tr] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int gq = (hb >> 2) + 4 * ch + q;
+          *reinterpret_cast<uint4*>(lrow + tr * kH + ((gq ^ (tr & 15)) << 2)) =
+              make_uint4(l[4 * q], l[4 * q + 1], l[4 * q + 2], l[4 * q + 3]);
+        }
       }
       if (xsync(false) < 0) break;
       float lsum = 0.0f, mrow = -INFINITY;
-      if (tr < kH && had) {
-        lsum = red_part[tr];
-        mrow = red_m[tr];
+      if (sid < kH) {
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 4
+        for (int r = 0; r < kBN; ++r) acc[r & 3] += lrow[r * kH + ((((sid >> 2) ^ (r & 15))) << 2) + (sid & 3)];
+        if (had) {
+          lsum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+          mrow = red_m[sid];
+        }
       }
+      if (xsync(false) < 0) break;  // the block is read before anyone reuses the P buffers
       if (kind == kPart) {
         // publish (O^T, m, l) of this part in workspace slot b
-        if (tr < kH) {
-          p.ws_ml[((int64_t)b * 2 + 0) * kH + tr] = mrow;
-          p.ws_ml[((int64_t)b * 2 + 1) * kH + tr] = lsum;
+        if (sid < kH) {
+          p.ws_ml[((int64_t)b * 2 + 0) * kH + sid] = mrow;
+          p.ws_ml[((int64_t)b * 2 + 1) * kH + sid] = lsum;
         }
         if (had) {
-          float* w0 = p.ws_o + ((int64_t)b * kD + tr) * kH;
-          float* w1 = p.ws_o + ((int64_t)b * kD + 128 + tr) * kH;
+          float* w0 = p.ws_o + ((int64_t)b * kD + tr) * kH + hb;
+          float* w1 = p.ws_o + ((int64_t)b * kD + 128 + tr) * kH + hb;
 #pragma unroll 1
-          for (int ch = 0; ch < 4; ++ch) {
+          for (int ch = 0; ch < kCH; ++ch) {
             uint32_t o0[16], o1[16];
-            tmem_ld32_x16(tl + C::O_COL + 16 * ch, o0);
-            tmem_ld32_x16(tl + C::O_COL + 64 + 16 * ch, o1);
+            tmem_ld32_x16(tl + C::O_COL + hb + 16 * ch, o0);
+            tmem_ld32_x16(tl + C::O_COL + 64 + hb + 16 * ch, o1);
             tc_wait_ld();
 #pragma unroll
             for (int i = 0; i < 16; i += 4) {
@@ -734,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __threadfence();
         __syncwarp();
         if (lane == 0)
-          asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.flags + 4 * b + sp), "r"(p.epoch) : "memory");
+          asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.flags + 8 * b + sm), "r"(p.epoch) : "memory");
         tc_fence_before();
         continue;
       }
@@ -742,11 +763,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nparts = kind == kHead ? last - b : 0;
       bool okp = true;
       for (int k = 1; k <= nparts && okp; ++k) {
-        for (int j = 0; j < 4 && okp; ++j) {
+        for (int j = 0; j < kNSM && okp; ++j) {
           int v = 0;
           const uint64_t t0 = globaltimer_ns();
           for (;;) {
-            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p.flags + 4 * (b + k) + j) : "memory");
+            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p.flags + 8 * (b + k) + j) : "memory");
             if (v == p.epoch || globaltimer_ns() - t0 > kWaitNs) break;
             __nanosleep(64);
           }
@@ -756,34 +777,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!okp) fail(DSA_DEVERR_TIMEOUT);
       // (the launch keeps nparts <= kMaxParts; more would overrun the weight table)
       const int np = (okp && nparts <= kMaxParts) ? nparts : 0;
-      if (tr < kH) {
+      if (sid < kH) {
         float M = mrow;
-        for (int k = 1; k <= np; ++k) M = fmaxf(M, p.ws_ml[((int64_t)(b + k) * 2 + 0) * kH + tr]);
+        for (int k = 1; k <= np; ++k) M = fmaxf(M, p.ws_ml[((int64_t)(b + k) * 2 + 0) * kH + sid]);
         const float w_own = lsum > 0.0f ? exp2f(mrow - M) : 0.0f;
         float L = w_own * lsum;
         for (int k = 1; k <= np; ++k) {
-          const float mk = p.ws_ml[((int64_t)(b + k) * 2 + 0) * kH + tr];
-          const float lk = p.ws_ml[((int64_t)(b + k) * 2 + 1) * kH + tr];
+          const float mk = p.ws_ml[((int64_t)(b + k) * 2 + 0) * kH + sid];
+          const float lk = p.ws_ml[((int64_t)(b + k) * 2 + 1) * kH + sid];
           const float wk = lk > 0.0f ? exp2f(mk - M) : 0.0f;
-          red_wk[(k - 1) * kH + tr] = wk;
+          red_wk[(k - 1) * kH + sid] = wk;
           L += wk * lk;
         }
         const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-        red_alpha[tr] = w_own * inv;
-        for (int k = 1; k <= np; ++k) red_wk[(k - 1) * kH + tr] *= inv;
-        if (p.lse) p.lse[t * kH + tr] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+        red_alpha[sid] = w_own * inv;
+        for (int k = 1; k <= np; ++k) red_wk[(k - 1) * kH + sid] *= inv;
+        if (p.lse) p.lse[t * kH + sid] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
       }
       if (xsync(false) < 0) break;
       // combine and stage the bf16 block [64 heads][256 columns] in the (idle) P buffers
       uint16_t* stage = reinterpret_cast<uint16_t*>(smem + C::P_OFF);
 #pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 0; ch < kCH; ++ch) {
+        const int h0 = hb + 16 * ch;
         float acc0[16], acc1[16];
-        const float* wo = red_alpha + 16 * ch;
+        const float* wo = red_alpha + h0;
         if (had) {
           uint32_t o0[16], o1[16];
-          tmem_ld32_x16(tl + C::O_COL + 16 * ch, o0);
-          tmem_ld32_x16(tl + C::O_COL + 64 + 16 * ch, o1);
+          tmem_ld32_x16(tl + C::O_COL + h0, o0);
+          tmem_ld32_x16(tl + C::O_COL + 64 + h0, o1);
           tc_wait_ld();
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -795,9 +817,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 16; ++i) acc0[i] = acc1[i] = 0.0f;
         }
         for (int k = 1; k <= np; ++k) {
-          const float* wk = red_wk + (k - 1) * kH + 16 * ch;
-          const float* s0 = p.ws_o + ((int64_t)(b + k) * kD + tr) * kH + 16 * ch;
-          const float* s1 = p.ws_o + ((int64_t)(b + k) * kD + 128 + tr) * kH + 16 * ch;
+          const float* wk = red_wk + (k - 1) * kH + h0;
+          const float* s0 = p.ws_o + ((int64_t)(b + k) * kD + tr) * kH + h0;
+          const float* s1 = p.ws_o + ((int64_t)(b + k) * kD + 128 + tr) * kH + h0;
 #pragma unroll
           for (int i = 0; i < 16; i += 4) {
             const float4 x = *reinterpret_cast<const float4*>(s0 + i);
@@ -814,29 +836,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          stage[(16 * ch + i) * kD + tr] = __bfloat16_as_ushort(__float2bfloat16_rn(acc0[i]));
-          stage[(16 * ch + i) * kD + 128 + tr] = __bfloat16_as_ushort(__float2bfloat16_rn(acc1[i]));
+          stage[(h0 + i) * kD + tr] = __bfloat16_as_ushort(__float2bfloat16_rn(acc0[i]));
+          stage[(h0 + i) * kD + 128 + tr] = __bfloat16_as_ushort(__float2bfloat16_rn(acc1[i]));
         }
       }
       if (xsync(false) < 0) break;
-      // copy out: 2048 16-byte granules (64 rows of 512 bytes), 16 per thread, row-contiguous
+      // copy out: 2048 16-byte granules (64 rows of 512 bytes), 8 per thread, row-contiguous
       {
         uint16_t* orow = p.out + t * p.out_st;
 #pragma unroll 4
-        for (int j = 0; j < 16; ++j) {
-          const int q = tr + 128 * j, h = q >> 5, gq = q & 31;
+        for (int j = 0; j < 2048 / (32 * kNSM); ++j) {
+          const int q = sid + 32 * kNSM * j, h = q >> 5, gq = q & 31;
           *reinterpret_cast<uint4*>(orow + (int64_t)h * p.out_sh + gq * 8) =
               *reinterpret_cast<const uint4*>(stage + h * kD + gq * 8);
         }
       }
       tc_fence_before();
     }
-  } else if (warp >= 8) {
-    // ====================================================== row loaders (8 warps) ====
-    // Warp dw fills rows dw, dw + 8, ... of each K tile in the 128-byte-swizzled K-major layout
+  } else if (loader_index(warp) >= 0) {
+    // ====================================================== row loaders (9 warps) ====
+    // Warp dw fills rows dw, dw + 4, ... of each K tile in the 128-byte-swizzled K-major layout
     // (row r, 16-byte granule q of 64-column chunk c at c*128*128 + r*128 + ((q ^ (r&7)) << 4)).
     // Rows past n_valid are zero (their keys are masked: a zero row keeps 0 * V finite).
-    const int dw = warp - 8;
+    const int dw = loader_index(warp);
+    const int nk = (kBN - dw + kNLD - 1) / kNLD;  // rows of this warp per tile: dw + kNLD * k, k < nk
     uint32_t mc = 0, g = 0;
     if constexpr (!C::FP8) {
       while (!*abort_flag) {
@@ -859,7 +882,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // one 512-byte row per warp-instruction: lane q copies granule q (chunk q/8, granule q%8)
         const int ch = lane >> 3, gr = lane & 7;
 #pragma unroll 4
-        for (int k = 0; k < kRPW; ++k) {
+        for (int k = 0; k < nk; ++k) {
           const int r = dw + kNLD * k;
           const bool v = r < n_valid;
           const uint8_t* row = p.cache + (v ? (int64_t)slots[r] : 0) * (2 * kD);
@@ -875,18 +898,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++g;
       }
     } else {
-      // Packed rows, two tiles in flight per warp: the loads of the next tile are issued before
-      // the current one is widened and stored. Lane l holds codes 8l .. 8l+7 of each of its
-      // rows; lanes 0-15 hold the two tile scales of row dw + 8 * lane.
-      struct Rows {
-        uint2 c[kRPW];
-        float2 sc;
-        int n_valid;
-      };
-      // fetch() waits for the next tile's slot list (skipping segment ends), issues its loads and
-      // releases the meta entry. It returns 1 when a tile was fetched, 0 at the end of the
-      // stream, and -1 (only when `block` is false) when the next entry is not published yet.
-      auto fetch = [&](Rows& R, bool block) -> int {
+      // Packed rows, two per copy instruction: the half-warp h of a row pair copies a 16-byte
+      // aligned 256-byte window of its row ([start, start+256) for even slots, [start-8,
+      // start+248) for odd ones, whose rows start 8 bytes past a 16-byte boundary) into a
+      // shared-memory ring (kRing rows in flight per warp, one commit group per pair), and the
+      // rolled widening loop waits for the oldest pair, widens each lane's 16 codes (two output
+      // granules; an odd row's window is shifted by one granule) and refills the pair's slots
+      // kRing/2 pairs later (of this tile or, once its entry is published, of the next one).
+      // Per tile, lane t also loads row t's tail: its two scales and, for an odd row, its last 8
+      // codes ([start+248, start+264); an even row reads only [start+256, start+264)).
+      constexpr int kPA = kRing / 2;  // pairs in flight
+      const int npairs = (nk + 1) / 2;
+      const int hl = lane >> 4, il = lane & 15;
+      const uint32_t ring_s = smem_u32(smem + C::RING_OFF + dw * (kRing * 256)) + hl * 256 + 16 * il;
+      const uint8_t* ring_g = smem + C::RING_OFF + dw * (kRing * 256) + hl * 256 + 16 * il;
+      auto next_tile = [&](bool block, int& st_out) -> int {
         while (!*abort_flag) {
           const int st = mc % kMST;
           if (!block && !mbar_test(m_full(st), (mc / kMST) & 1)) return -1;
@@ -894,71 +920,149 @@ __global__ void __launch_bounds__(kThreads, 1)
           const MetaHdr* mh = reinterpret_cast<const MetaHdr*>(smem + C::META_OFF + st * C::META_BYTES);
           const int type = mh->type;
           if (type == kTile) {
-            const int n = mh->n_valid;
-            R.n_valid = n;
-            const int* slots = reinterpret_cast<const int*>(reinterpret_cast<const uint8_t*>(mh) + 32);
-#pragma unroll
-            for (int k = 0; k < kRPW; ++k) {
-              const int r = dw + kNLD * k;
-              if (r < n) R.c[k] = __ldg(reinterpret_cast<const uint2*>(p.cache + (int64_t)slots[r] * C::RB + 8 * lane));
-            }
-            const int rs = dw + kNLD * lane;
-            R.sc = (lane < kRPW && rs < n)
-                       ? __ldg(reinterpret_cast<const float2*>(p.cache + (int64_t)slots[rs] * C::RB + kD))
-                       : make_float2(0.0f, 0.0f);
+            st_out = st;
+            return 1;
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(m_empty(st));
           ++mc;
-          if (type == kTile) return 1;
           if (type == kDone) return 0;
         }
         return 0;
       };
-      // widen the rows of R into the next K stage (and their scales), then publish it
-      auto convert = [&](const Rows& R) -> bool {
+      // tile in meta slot st: row count, and lane t's tail of row t (codes 248..255 of an odd
+      // row, the two scales)
+      auto take = [&](int st, int& n, uint2& tail, float2& scale, int& todd) {
+        const MetaHdr* mh = reinterpret_cast<const MetaHdr*>(smem + C::META_OFF + st * C::META_BYTES);
+        n = mh->n_valid;
+        const int* slots = reinterpret_cast<const int*>(reinterpret_cast<const uint8_t*>(mh) + 32);
+        const int rt = dw + kNLD * lane;
+        tail = make_uint2(0u, 0u);
+        scale = make_float2(0.0f, 0.0f);
+        todd = 0;
+        if (lane < nk && rt < n) {
+          const int sl = slots[rt];
+          todd = sl & 1;
+          const uint8_t* row = p.cache + (int64_t)sl * C::RB;
+          if (sl & 1) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(row + kD - 8));
+            tail = make_uint2(v.x, v.y);
+            scale = make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
+          } else {
+            scale = __ldg(reinterpret_cast<const float2*>(row + kD));
+          }
+        }
+      };
+      auto release = [&]() {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(m_empty(mc % kMST));
+        ++mc;
+      };
+      // copy pair j of the tile in meta slot st (n valid rows; st < 0: none) into ring pair
+      // q % kPA (q counts pairs across tiles), as one commit group; sets this lane's row parity
+      // bit in `par`
+      auto copy_pair = [&](int st, int n, int j, uint32_t q, uint32_t& par) {
+        const int k = 2 * j + hl, r = dw + kNLD * k;
+        if (st >= 0 && k < nk && r < n) {
+          const int sl = reinterpret_cast<const int*>(smem + C::META_OFF + st * C::META_BYTES + 32)[r];
+          par |= (uint32_t)(sl & 1) << k;
+          const uint8_t* src = p.cache + (((int64_t)sl * C::RB) & ~int64_t(15)) + 16 * il;
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(ring_s + (q % kPA) * 512), "l"(src) : "memory");
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+      };
+      int st_c = 0, n_c = 0, st_n = -1, n_n = 0;
+      uint32_t par_c = 0, par_n = 0;
+      uint2 tail_c = make_uint2(0u, 0u), tail_n = make_uint2(0u, 0u);
+      float2 sc_c = make_float2(0.0f, 0.0f), sc_n = make_float2(0.0f, 0.0f);
+      int todd_c = 0, todd_n = 0;  // this lane's tail row is an odd slot
+      uint32_t base = 0;           // pairs widened so far (ring position of the tile's pair 0)
+      int r = next_tile(true, st_c);
+      if (r == 1) {
+        take(st_c, n_c, tail_c, sc_c, todd_c);
+#pragma unroll 1
+        for (int j = 0; j < kPA; ++j) copy_pair(st_c, n_c, j, base + j, par_c);
+        if (npairs == kPA) release();
+      }
+      while (r == 1) {
         const int ks = g % kKST;
         uint8_t* kt = smem + C::KT_OFF + ks * C::KT_BYTES;
-        if (g >= (uint32_t)kKST && !wait(k_empty(ks), ((g / kKST) & 1) ^ 1)) return false;
-        const int ch = lane >> 3, gr = lane & 7;
-#pragma unroll
-        for (int k = 0; k < kRPW; ++k) {
-          const int r = dw + kNLD * k;
-          uint4 o = make_uint4(0, 0, 0, 0);
-          if (r < R.n_valid) {
-            o.x = e4m3x2_to_bf16x2_exact<0x9180u>(R.c[k].x);
-            o.y = e4m3x2_to_bf16x2_exact<0xB3A2u>(R.c[k].x);
-            o.z = e4m3x2_to_bf16x2_exact<0x9180u>(R.c[k].y);
-            o.w = e4m3x2_to_bf16x2_exact<0xB3A2u>(R.c[k].y);
+        if (g >= (uint32_t)kKST && !wait(k_empty(ks), ((g / kKST) & 1) ^ 1)) break;
+        bool have_n = false;
+        int look = -1;  // lookahead: 1 next tile taken, 0 end of stream, -1 not published
+        par_n = 0;
+#pragma unroll 1
+        for (int j = 0; j < npairs; ++j) {
+          asm volatile("cp.async.wait_group %0;" ::"n"(kPA - 1) : "memory");
+          const int k = 2 * j + hl, rr = dw + kNLD * k;
+          if (k < nk) {
+            const uint4 w = *reinterpret_cast<const uint4*>(ring_g + ((base + j) % kPA) * 512);
+            const bool v = rr < n_c;
+            const int odd = v ? (int)((par_c >> k) & 1u) : 0;
+            uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
+            if (v) {
+              o0 = make_uint4(e4m3x2_to_bf16x2_exact<0x9180u>(w.x), e4m3x2_to_bf16x2_exact<0xB3A2u>(w.x),
+                              e4m3x2_to_bf16x2_exact<0x9180u>(w.y), e4m3x2_to_bf16x2_exact<0xB3A2u>(w.y));
+              o1 = make_uint4(e4m3x2_to_bf16x2_exact<0x9180u>(w.z), e4m3x2_to_bf16x2_exact<0xB3A2u>(w.z),
+                              e4m3x2_to_bf16x2_exact<0x9180u>(w.w), e4m3x2_to_bf16x2_exact<0xB3A2u>(w.w));
+            }
+            uint8_t* rowk = kt + rr * 128;
+            const int sw = rr & 7;
+            const int g0 = 2 * il - odd, g1 = g0 + 1;  // output granules (8 codes each)
+            if (g0 >= 0) *reinterpret_cast<uint4*>(rowk + (g0 >> 3) * (kBN * 128) + (((g0 & 7) ^ sw) << 4)) = o0;
+            *reinterpret_cast<uint4*>(rowk + (g1 >> 3) * (kBN * 128) + (((g1 & 7) ^ sw) << 4)) = o1;
           }
-          *reinterpret_cast<uint4*>(kt + ch * (kBN * 128) + r * 128 + ((gr ^ (r & 7)) << 4)) = o;
+          __syncwarp();  // every lane has read ring pair j before it is refilled
+          const int jn = j + kPA;
+          if (jn < npairs) {
+            copy_pair(st_c, n_c, jn, base + jn, par_c);
+            if (jn == npairs - 1) release();  // all of this tile's pairs are copied
+          } else {
+            if (jn == npairs) {
+              int stx = -1;
+              look = next_tile(false, stx);
+              if (look == 1) {
+                st_n = stx;
+                take(st_n, n_n, tail_n, sc_n, todd_n);
+                have_n = true;
+              }
+            }
+            copy_pair(have_n ? st_n : -1, n_n, jn - npairs, base + jn, par_n);
+            if (have_n && jn - npairs == npairs - 1) release();
+          }
         }
-        if (lane < kRPW)
-          *reinterpret_cast<float2*>(smem + C::SC_OFF + ks * C::SC_BYTES + (dw + kNLD * lane) * 8) = R.sc;
+        // tails: the last granule of odd rows, and the scales
+        if (lane < nk) {
+          const int rt = dw + kNLD * lane;
+          if (rt < n_c && todd_c) {
+            const uint4 o = make_uint4(e4m3x2_to_bf16x2_exact<0x9180u>(tail_c.x), e4m3x2_to_bf16x2_exact<0xB3A2u>(tail_c.x),
+                                       e4m3x2_to_bf16x2_exact<0x9180u>(tail_c.y), e4m3x2_to_bf16x2_exact<0xB3A2u>(tail_c.y));
+            *reinterpret_cast<uint4*>(kt + 3 * (kBN * 128) + rt * 128 + ((7 ^ (rt & 7)) << 4)) = o;
+          }
+          *reinterpret_cast<float2*>(smem + C::SC_OFF + ks * C::SC_BYTES + rt * 8) = sc_c;
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(k_full(ks));
         ++g;
-        return true;
-      };
-      // The next tile is fetched ahead only when its entry is already published: waiting for it
-      // before storing the current tile could deadlock at a segment boundary (the next segment's
-      // first entry waits for its Q buffer, i.e. for this tile's score product). One fetch and
-      // one convert site: ra holds the fetched, not yet stored tile (when have_a), rb the next.
-      Rows ra, rb;
-      bool have_a = false;
-      for (;;) {
-        const int r = fetch(rb, !have_a);  // block only when there is nothing to store meanwhile
-        if (have_a) {
-          if (!convert(ra)) break;
-          have_a = false;
+        base += npairs;
+        if (have_n) {
+          st_c = st_n;
+          n_c = n_n;
+          par_c = par_n;
+          tail_c = tail_n;
+          sc_c = sc_n;
+          todd_c = todd_n;
+          continue;
         }
-        if (r == 1) {
-          ra = rb;
-          have_a = true;
-        } else if (r == 0) {
-          break;
-        }
+        if (look == 0) break;  // the lookahead already consumed the end of the stream
+        r = next_tile(true, st_c);
+        if (r != 1) break;
+        take(st_c, n_c, tail_c, sc_c, todd_c);
+        par_c = 0;
+#pragma unroll 1
+        for (int j = 0; j < kPA; ++j) copy_pair(st_c, n_c, j, base + j, par_c);
+        if (npairs == kPA) release();
       }
     }
     // drain this thread's outstanding cp.async copies before the CTA can finish
