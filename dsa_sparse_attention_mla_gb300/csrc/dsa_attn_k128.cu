@@ -902,13 +902,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // aligned 256-byte window of its row ([start, start+256) for even slots, [start-8,
       // start+248) for odd ones, whose rows start 8 bytes past a 16-byte boundary) into a
       // shared-memory ring (kRing rows in flight per warp, one commit group per pair), and the
-      // rolled widening loop waits for the oldest pair, widens each lane's 16 codes (two output
-      // granules; an odd row's window is shifted by one granule) and refills the pair's slots
-      // kRing/2 pairs later (of this tile or, once its entry is published, of the next one).
+      // rolled widening loop, two pairs a step, waits for the oldest two, widens each lane's 16
+      // codes (two output granules; an odd row's window is shifted by one granule) and refills
+      // their slots kRing/2 pairs later (of this tile or, once its entry is published, of the
+      // next one). Every warp walks 8 pairs per tile, so a tile starts at the same ring pair.
       // Per tile, lane t also loads row t's tail: its two scales and, for an odd row, its last 8
       // codes ([start+248, start+264); an even row reads only [start+256, start+264)).
       constexpr int kPA = kRing / 2;  // pairs in flight
-      const int npairs = (nk + 1) / 2;
+      constexpr int npairs = 8;       // pairs per tile for every warp (rows past nk are empty)
+      static_assert((kBN + kNLD - 1) / kNLD <= 2 * npairs && npairs % 2 == 0 && npairs > kPA, "loader pairs");
       const int hl = lane >> 4, il = lane & 15;
       const uint32_t ring_s = smem_u32(smem + C::RING_OFF + dw * (kRing * 256)) + hl * 256 + 16 * il;
       const uint8_t* ring_g = smem + C::RING_OFF + dw * (kRing * 256) + hl * 256 + 16 * il;
@@ -982,7 +984,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         take(st_c, n_c, tail_c, sc_c, todd_c);
 #pragma unroll 1
         for (int j = 0; j < kPA; ++j) copy_pair(st_c, n_c, j, base + j, par_c);
-        if (npairs == kPA) release();
       }
       while (r == 1) {
         const int ks = g % kKST;
@@ -992,43 +993,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         int look = -1;  // lookahead: 1 next tile taken, 0 end of stream, -1 not published
         par_n = 0;
 #pragma unroll 1
-        for (int j = 0; j < npairs; ++j) {
-          asm volatile("cp.async.wait_group %0;" ::"n"(kPA - 1) : "memory");
-          const int k = 2 * j + hl, rr = dw + kNLD * k;
-          if (k < nk) {
-            const uint4 w = *reinterpret_cast<const uint4*>(ring_g + ((base + j) % kPA) * 512);
-            const bool v = rr < n_c;
-            const int odd = v ? (int)((par_c >> k) & 1u) : 0;
-            uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
-            if (v) {
-              o0 = make_uint4(e4m3x2_to_bf16x2_exact<0x9180u>(w.x), e4m3x2_to_bf16x2_exact<0xB3A2u>(w.x),
-                              e4m3x2_to_bf16x2_exact<0x9180u>(w.y), e4m3x2_to_bf16x2_exact<0xB3A2u>(w.y));
-              o1 = make_uint4(e4m3x2_to_bf16x2_exact<0x9180u>(w.z), e4m3x2_to_bf16x2_exact<0xB3A2u>(w.z),
-                              e4m3x2_to_bf16x2_exact<0x9180u>(w.w), e4m3x2_to_bf16x2_exact<0xB3A2u>(w.w));
-            }
-            uint8_t* rowk = kt + rr * 128;
-            const int sw = rr & 7;
-            const int g0 = 2 * il - odd, g1 = g0 + 1;  // output granules (8 codes each)
-            if (g0 >= 0) *reinterpret_cast<uint4*>(rowk + (g0 >> 3) * (kBN * 128) + (((g0 & 7) ^ sw) << 4)) = o0;
-            *reinterpret_cast<uint4*>(rowk + (g1 >> 3) * (kBN * 128) + (((g1 & 7) ^ sw) << 4)) = o1;
-          }
-          __syncwarp();  // every lane has read ring pair j before it is refilled
-          const int jn = j + kPA;
-          if (jn < npairs) {
-            copy_pair(st_c, n_c, jn, base + jn, par_c);
-            if (jn == npairs - 1) release();  // all of this tile's pairs are copied
-          } else {
-            if (jn == npairs) {
-              int stx = -1;
-              look = next_tile(false, stx);
-              if (look == 1) {
-                st_n = stx;
-                take(st_n, n_n, tail_n, sc_n, todd_n);
-                have_n = true;
+        for (int j0 = 0; j0 < npairs; j0 += 2) {  // two pairs per step
+          asm volatile("cp.async.wait_group %0;" ::"n"(kPA - 2) : "memory");
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int j = j0 + u;
+            const int k = 2 * j + hl, rr = dw + kNLD * k;
+            if (k < nk) {
+              const uint4 w = *reinterpret_cast<const uint4*>(ring_g + ((base + j) % kPA) * 512);
+              const bool v = rr < n_c;
+              const int odd = v ? (int)((par_c >> k) & 1u) : 0;
+              uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
+              if (v) {
+                o0 = make_uint4(e4m3x2_to_bf16x2_exact<0x9180u>(w.x), e4m3x2_to_bf16x2_exact<0xB3A2u>(w.x),
+                                e4m3x2_to_bf16x2_exact<0x9180u>(w.y), e4m3x2_to_bf16x2_exact<0xB3A2u>(w.y));
+                o1 = make_uint4(e4m3x2_to_bf16x2_exact<0x9180u>(w.z), e4m3x2_to_bf16x2_exact<0xB3A2u>(w.z),
+                                e4m3x2_to_bf16x2_exact<0x9180u>(w.w), e4m3x2_to_bf16x2_exact<0xB3A2u>(w.w));
               }
+              uint8_t* rowk = kt + rr * 128;
+              const int sw = rr & 7;
+              const int g0 = 2 * il - odd, g1 = g0 + 1;  // output granules (8 codes each)
+              if (g0 >= 0) *reinterpret_cast<uint4*>(rowk + (g0 >> 3) * (kBN * 128) + (((g0 & 7) ^ sw) << 4)) = o0;
+              *reinterpret_cast<uint4*>(rowk + (g1 >> 3) * (kBN * 128) + (((g1 & 7) ^ sw) << 4)) = o1;
             }
-            copy_pair(have_n ? st_n : -1, n_n, jn - npairs, base + jn, par_n);
-            if (have_n && jn - npairs == npairs - 1) release();
+          }
+          __syncwarp();  // every lane has read ring pairs j0, j0 + 1 before they are refilled
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int jn = j0 + u + kPA;
+            if (jn < npairs) {
+              copy_pair(st_c, n_c, jn, base + jn, par_c);
+              if (jn == npairs - 1) release();  // all of this tile's pairs are copied
+            } else {
+              if (jn == npairs) {
+                int stx = -1;
+                look = next_tile(false, stx);
+                if (look == 1) {
+                  st_n = stx;
+                  take(st_n, n_n, tail_n, sc_n, todd_n);
+                  have_n = true;
+                }
+              }
+              copy_pair(have_n ? st_n : -1, n_n, jn - npairs, base + jn, par_n);
+            }
           }
         }
         // tails: the last granule of odd rows, and the scales
@@ -1062,7 +1069,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         par_c = 0;
 #pragma unroll 1
         for (int j = 0; j < kPA; ++j) copy_pair(st_c, n_c, j, base + j, par_c);
-        if (npairs == kPA) release();
       }
     }
     // drain this thread's outstanding cp.async copies before the CTA can finish
