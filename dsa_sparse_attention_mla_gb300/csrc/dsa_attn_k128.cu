@@ -616,41 +616,47 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
 #pragma unroll 1
             for (int ch = 0; ch < kCH; ++ch) {
-              uint32_t o0[16], o1[16];
+              uint32_t o0[16], o1[16], lv[16];
               tmem_ld32_x16(tl + C::O_COL + hb + 16 * ch, o0);
               tmem_ld32_x16(tl + C::O_COL + 64 + hb + 16 * ch, o1);
+              tmem_ld32_x16(lcur + 16 * ch, lv);
               tc_wait_ld();
               const float* al = red_alpha + hb + 16 * ch;
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
                 o0[i] = f2u(u2f(o0[i]) * al[i]);
                 o1[i] = f2u(u2f(o1[i]) * al[i]);
+                lv[i] = f2u(u2f(lv[i]) * al[i]);
               }
               tmem_st32_x16(tl + C::O_COL + hb + 16 * ch, o0);
               tmem_st32_x16(tl + C::O_COL + 64 + hb + 16 * ch, o1);
+              tmem_st32_x16(lcur + 16 * ch, lv);  // the partial sums the pass reads next
             }
+            tc_wait_st();
           }
           // the pass: p = 2^(c * score - m) (one FFMA and one MUFU ex2 per score), partial row
-          // sums into the other TMEM buffer (scaled by alpha after a rescale), and P (packed
-          // rows: p * scale of each tile) as bf16 into this key's 128-byte row
+          // sums into the other TMEM buffer (a rescale has already scaled the buffer it reads),
+          // and P (packed rows: p * scale of each tile) as bf16 into this key's 128-byte row
           float xm = -INFINITY;
 #pragma unroll 1
           for (int ch = 0; ch < kCH; ++ch) {
+            float mv[16];  // running maxima of the chunk's heads, read ahead of the TMEM wait
+#pragma unroll
+            for (int i = 0; i < 16; i += 4)
+              *reinterpret_cast<float4*>(mv + i) = *reinterpret_cast<const float4*>(red_m + hb + 16 * ch + i);
             uint32_t a[16], bb[16], l[16];
             tmem_ld32_x16(sa + 16 * ch, a);
             if constexpr (C::FP8) tmem_ld32_x16(sa + 64 + 16 * ch, bb);
             if (!first) tmem_ld32_x16(lcur + 16 * ch, l);
             tc_wait_ld();
-            const float* mrow = red_m + hb + 16 * ch;
-            const float* al = red_alpha + hb + 16 * ch;
             float pr[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const float x = score(a, bb, i) - mrow[i];
+              const float x = score(a, bb, i) - mv[i];
               xm = fmaxf(xm, valid ? x : -INFINITY);
               pr[i] = valid ? ex2_approx(x) : 0.0f;
               float lv = pr[i];
-              if (!first) lv = exact ? fmaf(u2f(l[i]), al[i], pr[i]) : u2f(l[i]) + pr[i];
+              if (!first) lv = u2f(l[i]) + pr[i];
               l[i] = f2u(lv);
             }
             tmem_st32_x16(lnxt + 16 * ch, l);
@@ -932,9 +938,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return 0;
       };
-      // tile in meta slot st: row count, and lane t's tail of row t (codes 248..255 of an odd
-      // row, the two scales)
-      auto take = [&](int st, int& n, uint2& tail, float2& scale, int& todd) {
+      // tile in meta slot st: row count, lane t's slot of row dw + kNLD * t (-1 past the tile) and
+      // its tail (codes 248..255 of an odd row, the two scales). Everything the loader needs of
+      // the entry is then in registers, so the caller releases the meta stage right away.
+      auto take = [&](int st, int& n, uint2& tail, float2& scale, int& todd, int& slr) {
         const MetaHdr* mh = reinterpret_cast<const MetaHdr*>(smem + C::META_OFF + st * C::META_BYTES);
         n = mh->n_valid;
         const int* slots = reinterpret_cast<const int*>(reinterpret_cast<const uint8_t*>(mh) + 32);
@@ -942,8 +949,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tail = make_uint2(0u, 0u);
         scale = make_float2(0.0f, 0.0f);
         todd = 0;
+        slr = -1;
         if (lane < nk && rt < n) {
           const int sl = slots[rt];
+          slr = sl;
           todd = sl & 1;
           const uint8_t* row = p.cache + (int64_t)sl * C::RB;
           if (sl & 1) {
@@ -960,13 +969,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(m_empty(mc % kMST));
         ++mc;
       };
-      // copy pair j of the tile in meta slot st (n valid rows; st < 0: none) into ring pair
-      // q % kPA (q counts pairs across tiles), as one commit group; sets this lane's row parity
-      // bit in `par`
-      auto copy_pair = [&](int st, int n, int j, uint32_t q, uint32_t& par) {
-        const int k = 2 * j + hl, r = dw + kNLD * k;
-        if (st >= 0 && k < nk && r < n) {
-          const int sl = reinterpret_cast<const int*>(smem + C::META_OFF + st * C::META_BYTES + 32)[r];
+      // copy pair j of a tile (slr: the slots `take` left in the lanes, or -1 for none) into
+      // ring pair q % kPA (q counts pairs across tiles), as one commit group; sets this lane's
+      // row parity bit in `par`. The slot of row k comes from lane k by a shuffle: no shared
+      // memory round trip on the way to the copy.
+      auto copy_pair = [&](int slr, int j, uint32_t q, uint32_t& par) {
+        const int k = 2 * j + hl;
+        const int sl = __shfl_sync(0xffffffffu, slr, k);
+        if (sl >= 0) {
           par |= (uint32_t)(sl & 1) << k;
           const uint8_t* src = p.cache + (((int64_t)sl * C::RB) & ~int64_t(15)) + 16 * il;
           asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(ring_s + (q % kPA) * 512), "l"(src) : "memory");
@@ -978,12 +988,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint2 tail_c = make_uint2(0u, 0u), tail_n = make_uint2(0u, 0u);
       float2 sc_c = make_float2(0.0f, 0.0f), sc_n = make_float2(0.0f, 0.0f);
       int todd_c = 0, todd_n = 0;  // this lane's tail row is an odd slot
+      int sl_c = -1, sl_n = -1;    // this lane's slot (row dw + kNLD * lane)
       uint32_t base = 0;           // pairs widened so far (ring position of the tile's pair 0)
       int r = next_tile(true, st_c);
       if (r == 1) {
-        take(st_c, n_c, tail_c, sc_c, todd_c);
+        take(st_c, n_c, tail_c, sc_c, todd_c, sl_c);
+        release();
 #pragma unroll 1
-        for (int j = 0; j < kPA; ++j) copy_pair(st_c, n_c, j, base + j, par_c);
+        for (int j = 0; j < kPA; ++j) copy_pair(sl_c, j, base + j, par_c);
       }
       while (r == 1) {
         const int ks = g % kKST;
@@ -995,12 +1007,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
         for (int j0 = 0; j0 < npairs; j0 += 2) {  // two pairs per step
           asm volatile("cp.async.wait_group %0;" ::"n"(kPA - 2) : "memory");
+          uint4 wv[2];  // both ring reads before any widening: one shared-memory round trip
+#pragma unroll
+          for (int u = 0; u < 2; ++u) wv[u] = *reinterpret_cast<const uint4*>(ring_g + ((base + j0 + u) % kPA) * 512);
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const int j = j0 + u;
             const int k = 2 * j + hl, rr = dw + kNLD * k;
             if (k < nk) {
-              const uint4 w = *reinterpret_cast<const uint4*>(ring_g + ((base + j) % kPA) * 512);
+              const uint4 w = wv[u];
               const bool v = rr < n_c;
               const int odd = v ? (int)((par_c >> k) & 1u) : 0;
               uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
@@ -1022,19 +1037,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int u = 0; u < 2; ++u) {
             const int jn = j0 + u + kPA;
             if (jn < npairs) {
-              copy_pair(st_c, n_c, jn, base + jn, par_c);
-              if (jn == npairs - 1) release();  // all of this tile's pairs are copied
+              copy_pair(sl_c, jn, base + jn, par_c);
             } else {
               if (jn == npairs) {
                 int stx = -1;
                 look = next_tile(false, stx);
                 if (look == 1) {
                   st_n = stx;
-                  take(st_n, n_n, tail_n, sc_n, todd_n);
+                  take(st_n, n_n, tail_n, sc_n, todd_n, sl_n);
+                  release();
                   have_n = true;
                 }
               }
-              copy_pair(have_n ? st_n : -1, n_n, jn - npairs, base + jn, par_n);
+              copy_pair(have_n ? sl_n : -1, jn - npairs, base + jn, par_n);
             }
           }
         }
@@ -1060,15 +1075,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           tail_c = tail_n;
           sc_c = sc_n;
           todd_c = todd_n;
+          sl_c = sl_n;
           continue;
         }
         if (look == 0) break;  // the lookahead already consumed the end of the stream
         r = next_tile(true, st_c);
         if (r != 1) break;
-        take(st_c, n_c, tail_c, sc_c, todd_c);
+        take(st_c, n_c, tail_c, sc_c, todd_c, sl_c);
+        release();
         par_c = 0;
 #pragma unroll 1
-        for (int j = 0; j < kPA; ++j) copy_pair(st_c, n_c, j, base + j, par_c);
+        for (int j = 0; j < kPA; ++j) copy_pair(sl_c, j, base + j, par_c);
       }
     }
     // drain this thread's outstanding cp.async copies before the CTA can finish
