@@ -42,6 +42,30 @@ def _peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+def _recorded_traffic(workload):
+    """DRAM bytes per launch of the attention kernel for this workload, from the ncu capture
+    recorded under profiles/, or None when there is none or the kernel sources have changed
+    since it was taken (the record carries a hash of the sources it was measured on)."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    src = os.path.join(ROOT, "dsa_sparse_attention_mla_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(src)):
+        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
+            h.update(name.encode())
+            with open(os.path.join(src, name), "rb") as f:
+                h.update(f.read())
+    if h.hexdigest() != rec.get("csrc_sha256"):
+        return None
+    w = rec.get("workloads", {}).get(workload)
+    return None if w is None else int(w["traffic"])
+
+
 def algorithmic_work(wl):
     """Algorithmic bytes and FLOPs of one full call (per the data each token must touch once):
     gathered rows (valid entries x row bytes) + q + out + the index list + the block table;
@@ -344,7 +368,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": None, "peak_source": peak_src,
+                     "traffic": _recorded_traffic(wl.name), "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": work["bytes"], "tflops": tflops,
                      "tensor_frac_of_bf16_burst": tflops / bf16},
         "cpu_baseline": {"value": cpu_v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},

@@ -1,0 +1,37 @@
+"""Host-side pieces of bench.py: the algorithmic byte count and the recorded DRAM traffic."""
+import json
+
+
+import bench
+from dsa_sparse_attention_mla_gb300 import workloads as W
+
+
+def test_algorithmic_bytes_fp8_decode():
+    # valid rows x 264-byte packed rows + q + out + index list + block table
+    wl = W.config(3)
+    w = bench.algorithmic_work(wl)
+    n_valid = int((wl.indices >= 0).sum())
+    expect = n_valid * 264 + wl.T * 64 * 256 * 2 * 2 + wl.indices.size * 4 + wl.block_table.size * 4
+    assert w["bytes"] == expect
+    assert w["flops"] == 2.0 * 64 * n_valid * (256 + 256)
+
+
+def test_recorded_traffic_tracks_kernel_sources(tmp_path, monkeypatch):
+    # a record whose hash matches the sources is reported; any change to them voids it
+    root = tmp_path
+    src = root / "dsa_sparse_attention_mla_gb300" / "csrc"
+    src.mkdir(parents=True)
+    (src / "k.cu").write_text("kernel v1")
+    (root / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    import hashlib
+
+    h = hashlib.sha256()
+    h.update(b"k.cu")
+    h.update(b"kernel v1")
+    rec = {"csrc_sha256": h.hexdigest(), "workloads": {"w": {"traffic": 1234}}}
+    (root / "profiles" / "dram_traffic.json").write_text(json.dumps(rec))
+    assert bench._recorded_traffic("w") == 1234
+    assert bench._recorded_traffic("other") is None
+    (src / "k.cu").write_text("kernel v2")
+    assert bench._recorded_traffic("w") is None
