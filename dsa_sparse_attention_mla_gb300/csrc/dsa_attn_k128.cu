@@ -59,7 +59,7 @@ constexpr int kThreads = 32 * kWarps;
 // loader warp index (3 -> 0, 8..15 -> 1..8), -1 for other warps
 __device__ __forceinline__ int loader_index(int warp) { return warp == 3 ? 0 : (warp >= 8 ? warp - 7 : -1); }
 constexpr int kMaxParts = 16;     // most parts of one split token (the launch guarantees it)
-constexpr int kRing = 8;          // packed rows in flight per loader warp (shared-memory ring)
+constexpr int kRing = 8;          // ring of a packed-row loader warp: 2 units of 8 half rows (2 KB)
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 template <int KIND>
@@ -86,7 +86,7 @@ struct Cfg {
   // m[64], alpha[64], lsum[64], spare[64], part[4][64], wk[kMaxParts][64], votes[2][8]
   static constexpr int RED_FLOATS = 8 * kH + kMaxParts * kH + 2 * kNSM;
   static constexpr int BAR_OFF = RED_OFF + ((RED_FLOATS * 4 + 15) & ~15);
-  static constexpr int NBARS = 2 + 2 * kKST + 2 * kMST + 8 + 3;
+  static constexpr int NBARS = 2 + 4 * kKST + 2 * kMST + 8 + 3;
   static constexpr int MISC_OFF = BAR_OFF + 8 * NBARS;
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + alignment slack
   // tensor memory columns
@@ -178,11 +178,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const uint32_t bar0 = sbase + C::BAR_OFF;
   const uint32_t q_full = bar0, q_empty = bar0 + 8;
-  auto k_full = [&](int s) { return bar0 + 16 + 8 * s; };
-  auto k_empty = [&](int s) { return bar0 + 16 + 8 * (kKST + s); };
-  auto m_full = [&](int s) { return bar0 + 16 + 8 * (2 * kKST + s); };
-  auto m_empty = [&](int s) { return bar0 + 16 + 8 * (2 * kKST + kMST + s); };
-  const uint32_t x0 = bar0 + 16 + 8 * (2 * kKST + 2 * kMST);
+  // K stage s, column half h (codes / columns 0-127, 128-255): written, and free again
+  auto k_full = [&](int s, int h) { return bar0 + 16 + 8 * (2 * s + h); };
+  auto k_empty = [&](int s, int h) { return bar0 + 16 + 8 * (2 * kKST + 2 * s + h); };
+  auto m_full = [&](int s) { return bar0 + 16 + 8 * (4 * kKST + s); };
+  auto m_empty = [&](int s) { return bar0 + 16 + 8 * (4 * kKST + kMST + s); };
+  const uint32_t x0 = bar0 + 16 + 8 * (4 * kKST + 2 * kMST);
   auto s_full = [&](int i) { return x0 + 8 * i; };
   auto s_empty = [&](int i) { return x0 + 16 + 8 * i; };
   auto p_full = [&](int i) { return x0 + 32 + 8 * i; };
@@ -196,9 +197,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     for (int s = 0; s < kKST; ++s) {
-      // bf16 rows: one cp.async arrive per loader thread; packed rows: one arrive per loader warp
-      mbar_init(k_full(s), C::FP8 ? kNLD : 32 * kNLD);
-      mbar_init(k_empty(s), 1);
+      for (int h = 0; h < 2; ++h) {
+        // bf16 rows: one cp.async arrive per loader thread; packed rows: one per loader warp
+        mbar_init(k_full(s, h), C::FP8 ? kNLD : 32 * kNLD);
+        mbar_init(k_empty(s, h), 1);
+      }
     }
     for (int s = 0; s < kMST; ++s) {
       mbar_init(m_full(s), 1);
@@ -449,24 +452,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!wait(q_full, qc & 1)) break;
             ++qc;
           }
-          if (!wait(k_full(ks), (g / kKST) & 1)) break;
           if (g >= 2 && !wait(s_empty(g & 1), ((g >> 1) & 1) ^ 1)) break;
-          // bf16 rows arrive by cp.async (generic proxy): order them before the tensor core reads
-          // (the packed-row loaders fence on their side before arriving)
-          if constexpr (!C::FP8) fence_proxy_async_smem();
-          tc_fence_after();
           const uint32_t k_lo = (uint32_t)sw128_desc(sbase + C::KT_OFF + ks * C::KT_BYTES, 16, 1024);
           const uint32_t d0 = tmem + (g & 1) * C::S_COLS;
-#pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
-            // 16-column step kk: chunk kk/4 of 64 columns, 32 bytes per step inside the chunk
+          // 16-column step kk: chunk kk/4 of 64 columns, 32 bytes per step inside the chunk;
+          // packed rows accumulate columns 0-127 and 128-255 separately (one scale each)
+          auto step = [&](int kk) {
             const uint32_t ka = (uint32_t)((kk >> 2) * ((kBN * 128) >> 4) + (kk & 3) * 2);
             const uint32_t qa = (uint32_t)((kk >> 2) * ((kH * 128) >> 4) + (kk & 3) * 2);
-            // packed rows: columns 0-127 and 128-255 accumulate separately (one scale each)
             const uint32_t d = C::FP8 ? d0 + 64 * (kk >> 3) : d0;
             if ((C::FP8 ? (kk & 7) : kk) == 0) mma_bf16_lohi<0>(d, k_lo + ka, k_hi, q_lo + qa, q_hi, idS);
             else mma_bf16_lohi<1>(d, k_lo + ka, k_hi, q_lo + qa, q_hi, idS);
-          }
+          };
+          // the first column half's products start while the loaders write the second half
+          if (!wait(k_full(ks, 0), (g / kKST) & 1)) break;
+          // bf16 rows arrive by cp.async (generic proxy): order them before the tensor core
+          // reads (the packed-row loaders fence on their side before arriving)
+          if constexpr (!C::FP8) fence_proxy_async_smem();
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kD / 32; ++kk) step(kk);
+          if (!wait(k_full(ks, 1), (g / kKST) & 1)) break;
+          if constexpr (!C::FP8) fence_proxy_async_smem();
+          tc_fence_after();
+#pragma unroll
+          for (int kk = kD / 32; kk < kD / 16; ++kk) step(kk);
           mma_commit(s_full(g & 1));
         } else {
           // ---- output O^T += V^T P^T for tile g, once its probabilities are written
@@ -486,8 +496,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_bf16(d, ((uint64_t)mn_hi << 32) | va, ((uint64_t)mn_hi << 32) | pa, idPV, first ? 0u : 1u);
 #pragma unroll
             for (int j = 1; j < kBN / 16; ++j) mma_bf16_lohi<1>(d, va + 128 * j, mn_hi, pa + 128 * j, mn_hi, idPV);
+            // d_v half h has read columns 128h .. 128h + 127 of the K tile: that half is free
+            mma_commit(k_empty(ks, h));
           }
-          mma_commit(k_empty(ks));
           mma_commit(pv_done(g & 1));
         }
         ++g;
@@ -516,7 +527,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* red = reinterpret_cast<float*>(smem + C::RED_OFF);
     float* red_m = red;           // running max per head (exp2 domain)
     float* red_alpha = red + 64;  // rescale factor per head; epilogue: weight of own partial
-    float* red_l = red + 128;     // epilogue: row sum per head
     float* red_part = red + 256;  // [4 lane quarters][64 heads]
     float* red_wk = red + 512;    // [kMaxParts][64]: merge weights of the other parts
     int* votes = reinterpret_cast<int*>(red + 512 + kMaxParts * kH);  // [2][kNSM]
@@ -555,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ks = g % kKST;
         bool ok = mbar_wait(s_full(g & 1), (g >> 1) & 1, kWaitNs);
         // the tile scales come from the loaders: acquire their stage barrier directly
-        if constexpr (C::FP8) ok = ok && mbar_wait(k_full(ks), (g / kKST) & 1, kWaitNs);
+        if constexpr (C::FP8) ok = ok && mbar_wait(k_full(ks, 1), (g / kKST) & 1, kWaitNs);
         // the P buffer must be free: the PV product that read it last is complete
         ok = ok && pv_wait((int64_t)g - C::PBUF);
         if (!wait_all(ok)) break;
@@ -861,231 +871,195 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (loader_index(warp) >= 0) {
     // ====================================================== row loaders (9 warps) ====
-    // Warp dw fills rows dw, dw + 4, ... of each K tile in the 128-byte-swizzled K-major layout
-    // (row r, 16-byte granule q of 64-column chunk c at c*128*128 + r*128 + ((q ^ (r&7)) << 4)).
+    // Warp dw fills rows dw + kNLD * k (k < nk) of each K tile in the 128-byte-swizzled K-major
+    // layout (row r, 16-byte granule q of 64-column chunk c at c*128*128 + r*128 + ((q ^ (r&7)) << 4)).
+    // A tile is written in two column halves, columns 0-127 (chunks 0-1) and 128-255 (chunks
+    // 2-3), each with its own full and empty barrier: the score product starts on the first half
+    // while the second is written, and a stage's first half is refilled as soon as the output
+    // product's first d_v half has read it. Rows are taken in pairs (lanes 0-15: row 2p,
+    // 16-31: row 2p + 1); lane il of a half warp handles 16-byte granule 16h + il of its row, so
+    // the eight lanes of a quarter warp store to eight different 16-byte positions.
     // Rows past n_valid are zero (their keys are masked: a zero row keeps 0 * V finite).
     const int dw = loader_index(warp);
     const int nk = (kBN - dw + kNLD - 1) / kNLD;  // rows of this warp per tile: dw + kNLD * k, k < nk
+    static_assert((kBN + kNLD - 1) / kNLD <= 16, "a warp's rows of a tile fit eight row pairs");
+    const int hl = lane >> 4, il = lane & 15;
     uint32_t mc = 0, g = 0;
-    if constexpr (!C::FP8) {
+    auto next_tile = [&](bool block, int& st_out) -> int {
       while (!*abort_flag) {
         const int st = mc % kMST;
-        if (!wait(m_full(st), (mc / kMST) & 1)) break;
+        if (!block && !mbar_test(m_full(st), (mc / kMST) & 1)) return -1;
+        if (!wait(m_full(st), (mc / kMST) & 1)) return 0;
         const MetaHdr* mh = reinterpret_cast<const MetaHdr*>(smem + C::META_OFF + st * C::META_BYTES);
         const int type = mh->type;
-        if (type != kTile) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(m_empty(st));
-          ++mc;
-          if (type == kDone) break;
-          continue;
-        }
-        const int n_valid = mh->n_valid;
-        const int* slots = reinterpret_cast<const int*>(reinterpret_cast<const uint8_t*>(mh) + 32);
-        const int ks = g % kKST;
-        uint8_t* kt = smem + C::KT_OFF + ks * C::KT_BYTES;
-        if (g >= (uint32_t)kKST && !wait(k_empty(ks), ((g / kKST) & 1) ^ 1)) break;
-        // one 512-byte row per warp-instruction: lane q copies granule q (chunk q/8, granule q%8)
-        const int ch = lane >> 3, gr = lane & 7;
-#pragma unroll 4
-        for (int k = 0; k < nk; ++k) {
-          const int r = dw + kNLD * k;
-          const bool v = r < n_valid;
-          const uint8_t* row = p.cache + (v ? (int64_t)slots[r] : 0) * (2 * kD);
-          const uint32_t dst = smem_u32(kt + ch * (kBN * 128) + r * 128 + ((gr ^ (r & 7)) << 4));
-          asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(row + 16 * lane),
-                       "r"(v ? 16 : 0)
-                       : "memory");
+        if (type == kTile) {
+          st_out = st;
+          return 1;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(m_empty(st));
         ++mc;
-        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(k_full(ks)) : "memory");
+        if (type == kDone) return 0;
+      }
+      return 0;
+    };
+    // tile in meta slot st: row count, lane t's slot of row dw + kNLD * t (-1 past the valid
+    // rows) and, for packed rows, its two scales. Everything the loader needs of the entry is
+    // then in registers: the caller releases the meta stage right away, and a copy takes the
+    // slot of row k from lane k by a shuffle.
+    auto take = [&](int st, int& n, int& slr, float2& scale) {
+      const MetaHdr* mh = reinterpret_cast<const MetaHdr*>(smem + C::META_OFF + st * C::META_BYTES);
+      n = mh->n_valid;
+      const int* slots = reinterpret_cast<const int*>(reinterpret_cast<const uint8_t*>(mh) + 32);
+      const int rt = dw + kNLD * lane;
+      slr = -1;
+      scale = make_float2(0.0f, 0.0f);
+      if (lane < nk && rt < n) {
+        slr = slots[rt];
+        if constexpr (C::FP8) scale = __ldg(reinterpret_cast<const float2*>(p.cache + (int64_t)slr * C::RB + kD));
+      }
+    };
+    auto release = [&]() {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(m_empty(mc % kMST));
+      ++mc;
+    };
+    if constexpr (!C::FP8) {
+      // bf16 rows: 16-byte cp.async straight into the tile, one row pair per instruction; each
+      // thread's copies of a half signal that half's full barrier when they land
+      int st = 0, n = 0, slr = -1;
+      float2 unused;
+      bool bad = false;
+      while (!bad && next_tile(true, st) == 1) {
+        take(st, n, slr, unused);
+        release();
+        const int ks = g % kKST;
+        uint8_t* kt = smem + C::KT_OFF + ks * C::KT_BYTES;
+        for (int h = 0; h < 2; ++h) {
+          if (g >= (uint32_t)kKST && !wait(k_empty(ks, h), ((g / kKST) & 1) ^ 1)) {
+            bad = true;
+            break;
+          }
+          const int G = 16 * h + il;
+#pragma unroll
+          for (int pp = 0; pp < 8; ++pp) {
+            const int k = 2 * pp + hl;
+            const int sl = __shfl_sync(0xffffffffu, slr, k);
+            if (k < nk) {
+              const int r = dw + kNLD * k;
+              const uint8_t* src = p.cache + (sl >= 0 ? (int64_t)sl : 0) * (2 * kD) + 16 * G;
+              const uint32_t dst = smem_u32(kt + (G >> 3) * (kBN * 128) + r * 128 + (((G & 7) ^ (r & 7)) << 4));
+              asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(sl >= 0 ? 16 : 0)
+                           : "memory");
+            }
+          }
+          asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(k_full(ks, h)) : "memory");
+        }
         ++g;
       }
     } else {
-      // Packed rows, two per copy instruction: the half-warp h of a row pair copies a 16-byte
-      // aligned 256-byte window of its row ([start, start+256) for even slots, [start-8,
-      // start+248) for odd ones, whose rows start 8 bytes past a 16-byte boundary) into a
-      // shared-memory ring (kRing rows in flight per warp, one commit group per pair), and the
-      // rolled widening loop, two pairs a step, waits for the oldest two, widens each lane's 16
-      // codes (two output granules; an odd row's window is shifted by one granule) and refills
-      // their slots kRing/2 pairs later (of this tile or, once its entry is published, of the
-      // next one). Every warp walks 8 pairs per tile, so a tile starts at the same ring pair.
-      // Per tile, lane t also loads row t's tail: its two scales and, for an odd row, its last 8
-      // codes ([start+248, start+264); an even row reads only [start+256, start+264)).
-      constexpr int kPA = kRing / 2;  // pairs in flight
-      constexpr int npairs = 8;       // pairs per tile for every warp (rows past nk are empty)
-      static_assert((kBN + kNLD - 1) / kNLD <= 2 * npairs && npairs % 2 == 0 && npairs > kPA, "loader pairs");
-      const int hl = lane >> 4, il = lane & 15;
-      const uint32_t ring_s = smem_u32(smem + C::RING_OFF + dw * (kRing * 256)) + hl * 256 + 16 * il;
-      const uint8_t* ring_g = smem + C::RING_OFF + dw * (kRing * 256) + hl * 256 + 16 * il;
-      auto next_tile = [&](bool block, int& st_out) -> int {
-        while (!*abort_flag) {
-          const int st = mc % kMST;
-          if (!block && !mbar_test(m_full(st), (mc / kMST) & 1)) return -1;
-          if (!wait(m_full(st), (mc / kMST) & 1)) return 0;
-          const MetaHdr* mh = reinterpret_cast<const MetaHdr*>(smem + C::META_OFF + st * C::META_BYTES);
-          const int type = mh->type;
-          if (type == kTile) {
-            st_out = st;
-            return 1;
+      // Packed rows, one column half at a time. A unit is four row pairs of one half (8 x 128
+      // codes = 1 KB); a lane copies 8 codes of its row by an 8-byte cp.async (a packed row is
+      // 8-byte aligned, so the copy carries exactly the codes it needs) into a two-unit ring
+      // per warp, one commit group per unit. A tile is four units: half 0 pairs 0-3 and 4-7,
+      // then half 1. The widening loop waits for the older unit, widens each lane's 8 codes per
+      // pair into one output granule, and refills the unit's ring slot with the unit two ahead,
+      // of this tile or (once its meta entry is published) of the next one.
+      const uint32_t ring_s = smem_u32(smem + C::RING_OFF + dw * 2048) + hl * 128 + 8 * il;
+      const uint8_t* ring_g = smem + C::RING_OFF + dw * 2048 + hl * 128 + 8 * il;
+      auto copy_unit = [&](int slr, int u) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int k = 2 * (4 * (u & 1) + q) + hl;
+          const int sl = __shfl_sync(0xffffffffu, slr, k);
+          if (sl >= 0) {
+            const uint8_t* src = p.cache + (int64_t)sl * C::RB + 128 * (u >> 1) + 8 * il;
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(ring_s + (u & 1) * 1024 + q * 256), "l"(src)
+                         : "memory");
           }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(m_empty(st));
-          ++mc;
-          if (type == kDone) return 0;
-        }
-        return 0;
-      };
-      // tile in meta slot st: row count, lane t's slot of row dw + kNLD * t (-1 past the tile) and
-      // its tail (codes 248..255 of an odd row, the two scales). Everything the loader needs of
-      // the entry is then in registers, so the caller releases the meta stage right away.
-      auto take = [&](int st, int& n, uint2& tail, float2& scale, int& todd, int& slr) {
-        const MetaHdr* mh = reinterpret_cast<const MetaHdr*>(smem + C::META_OFF + st * C::META_BYTES);
-        n = mh->n_valid;
-        const int* slots = reinterpret_cast<const int*>(reinterpret_cast<const uint8_t*>(mh) + 32);
-        const int rt = dw + kNLD * lane;
-        tail = make_uint2(0u, 0u);
-        scale = make_float2(0.0f, 0.0f);
-        todd = 0;
-        slr = -1;
-        if (lane < nk && rt < n) {
-          const int sl = slots[rt];
-          slr = sl;
-          todd = sl & 1;
-          const uint8_t* row = p.cache + (int64_t)sl * C::RB;
-          if (sl & 1) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(row + kD - 8));
-            tail = make_uint2(v.x, v.y);
-            scale = make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
-          } else {
-            scale = __ldg(reinterpret_cast<const float2*>(row + kD));
-          }
-        }
-      };
-      auto release = [&]() {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(m_empty(mc % kMST));
-        ++mc;
-      };
-      // copy pair j of a tile (slr: the slots `take` left in the lanes, or -1 for none) into
-      // ring pair q % kPA (q counts pairs across tiles), as one commit group; sets this lane's
-      // row parity bit in `par`. The slot of row k comes from lane k by a shuffle: no shared
-      // memory round trip on the way to the copy.
-      auto copy_pair = [&](int slr, int j, uint32_t q, uint32_t& par) {
-        const int k = 2 * j + hl;
-        const int sl = __shfl_sync(0xffffffffu, slr, k);
-        if (sl >= 0) {
-          par |= (uint32_t)(sl & 1) << k;
-          const uint8_t* src = p.cache + (((int64_t)sl * C::RB) & ~int64_t(15)) + 16 * il;
-          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(ring_s + (q % kPA) * 512), "l"(src) : "memory");
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
       };
-      int st_c = 0, n_c = 0, st_n = -1, n_n = 0;
-      uint32_t par_c = 0, par_n = 0;
-      uint2 tail_c = make_uint2(0u, 0u), tail_n = make_uint2(0u, 0u);
+      int st_c = 0, n_c = 0, st_n = -1, n_n = 0, sl_c = -1, sl_n = -1;
       float2 sc_c = make_float2(0.0f, 0.0f), sc_n = make_float2(0.0f, 0.0f);
-      int todd_c = 0, todd_n = 0;  // this lane's tail row is an odd slot
-      int sl_c = -1, sl_n = -1;    // this lane's slot (row dw + kNLD * lane)
-      uint32_t base = 0;           // pairs widened so far (ring position of the tile's pair 0)
+      bool have_n = false;
+      int look = -1;  // lookahead: 1 next tile taken, 0 end of stream, -1 not published yet
+      auto look_ahead = [&]() {
+        if (have_n || look == 0) return;
+        int stx = -1;
+        look = next_tile(false, stx);
+        if (look == 1) {
+          st_n = stx;
+          take(st_n, n_n, sl_n, sc_n);
+          release();
+          have_n = true;
+        }
+      };
       int r = next_tile(true, st_c);
       if (r == 1) {
-        take(st_c, n_c, tail_c, sc_c, todd_c, sl_c);
+        take(st_c, n_c, sl_c, sc_c);
         release();
-#pragma unroll 1
-        for (int j = 0; j < kPA; ++j) copy_pair(sl_c, j, base + j, par_c);
+        copy_unit(sl_c, 0);
+        copy_unit(sl_c, 1);
       }
       while (r == 1) {
+        look_ahead();  // the next tile's entry, while this one's stage may still be busy
         const int ks = g % kKST;
         uint8_t* kt = smem + C::KT_OFF + ks * C::KT_BYTES;
-        if (g >= (uint32_t)kKST && !wait(k_empty(ks), ((g / kKST) & 1) ^ 1)) break;
-        bool have_n = false;
-        int look = -1;  // lookahead: 1 next tile taken, 0 end of stream, -1 not published
-        par_n = 0;
+        const bool full = n_c == kBN;  // every row valid: no zero rows to write
+        bool bad = false;
 #pragma unroll 1
-        for (int j0 = 0; j0 < npairs; j0 += 2) {  // two pairs per step
-          asm volatile("cp.async.wait_group %0;" ::"n"(kPA - 2) : "memory");
-          uint4 wv[2];  // both ring reads before any widening: one shared-memory round trip
-#pragma unroll
-          for (int u = 0; u < 2; ++u) wv[u] = *reinterpret_cast<const uint4*>(ring_g + ((base + j0 + u) % kPA) * 512);
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int j = j0 + u;
-            const int k = 2 * j + hl, rr = dw + kNLD * k;
-            if (k < nk) {
-              const uint4 w = wv[u];
-              const bool v = rr < n_c;
-              const int odd = v ? (int)((par_c >> k) & 1u) : 0;
-              uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
-              if (v) {
-                o0 = make_uint4(e4m3x2_to_bf16x2_exact<0x9180u>(w.x), e4m3x2_to_bf16x2_exact<0xB3A2u>(w.x),
-                                e4m3x2_to_bf16x2_exact<0x9180u>(w.y), e4m3x2_to_bf16x2_exact<0xB3A2u>(w.y));
-                o1 = make_uint4(e4m3x2_to_bf16x2_exact<0x9180u>(w.z), e4m3x2_to_bf16x2_exact<0xB3A2u>(w.z),
-                                e4m3x2_to_bf16x2_exact<0x9180u>(w.w), e4m3x2_to_bf16x2_exact<0xB3A2u>(w.w));
-              }
-              uint8_t* rowk = kt + rr * 128;
-              const int sw = rr & 7;
-              const int g0 = 2 * il - odd, g1 = g0 + 1;  // output granules (8 codes each)
-              if (g0 >= 0) *reinterpret_cast<uint4*>(rowk + (g0 >> 3) * (kBN * 128) + (((g0 & 7) ^ sw) << 4)) = o0;
-              *reinterpret_cast<uint4*>(rowk + (g1 >> 3) * (kBN * 128) + (((g1 & 7) ^ sw) << 4)) = o1;
-            }
+        for (int u = 0; u < 4; ++u) {
+          const int h = u >> 1;
+          if ((u & 1) == 0 && g >= (uint32_t)kKST && !wait(k_empty(ks, h), ((g / kKST) & 1) ^ 1)) {
+            bad = true;
+            break;
           }
-          __syncwarp();  // every lane has read ring pairs j0, j0 + 1 before they are refilled
+          asm volatile("cp.async.wait_group 1;" ::: "memory");
+          uint2 w[4];  // all four ring reads first: one shared-memory round trip
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int jn = j0 + u + kPA;
-            if (jn < npairs) {
-              copy_pair(sl_c, jn, base + jn, par_c);
-            } else {
-              if (jn == npairs) {
-                int stx = -1;
-                look = next_tile(false, stx);
-                if (look == 1) {
-                  st_n = stx;
-                  take(st_n, n_n, tail_n, sc_n, todd_n, sl_n);
-                  release();
-                  have_n = true;
-                }
-              }
-              copy_pair(have_n ? sl_n : -1, jn - npairs, base + jn, par_n);
-            }
+          for (int q = 0; q < 4; ++q) w[q] = *reinterpret_cast<const uint2*>(ring_g + (u & 1) * 1024 + q * 256);
+          const int G = 16 * h + il;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int k = 2 * (4 * (u & 1) + q) + hl, rr = dw + kNLD * k;
+            uint4 o = make_uint4(e4m3x2_to_bf16x2_exact<0x9180u>(w[q].x), e4m3x2_to_bf16x2_exact<0xB3A2u>(w[q].x),
+                                 e4m3x2_to_bf16x2_exact<0x9180u>(w[q].y), e4m3x2_to_bf16x2_exact<0xB3A2u>(w[q].y));
+            if (!full && rr >= n_c) o = make_uint4(0u, 0u, 0u, 0u);
+            if (k < nk) *reinterpret_cast<uint4*>(kt + (G >> 3) * (kBN * 128) + rr * 128 + (((G & 7) ^ (rr & 7)) << 4)) = o;
+          }
+          __syncwarp();  // every lane has read the unit's ring slot before it is refilled
+          if (u < 2) {
+            copy_unit(sl_c, u + 2);
+          } else {
+            if (u == 2) look_ahead();
+            copy_unit(have_n ? sl_n : -1, u - 2);
+          }
+          if (u & 1) {  // column half h of the tile is written
+            if (h == 1 && lane < nk)
+              *reinterpret_cast<float2*>(smem + C::SC_OFF + ks * C::SC_BYTES + (dw + kNLD * lane) * 8) = sc_c;
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(k_full(ks, h));
           }
         }
-        // tails: the last granule of odd rows, and the scales
-        if (lane < nk) {
-          const int rt = dw + kNLD * lane;
-          if (rt < n_c && todd_c) {
-            const uint4 o = make_uint4(e4m3x2_to_bf16x2_exact<0x9180u>(tail_c.x), e4m3x2_to_bf16x2_exact<0xB3A2u>(tail_c.x),
-                                       e4m3x2_to_bf16x2_exact<0x9180u>(tail_c.y), e4m3x2_to_bf16x2_exact<0xB3A2u>(tail_c.y));
-            *reinterpret_cast<uint4*>(kt + 3 * (kBN * 128) + rt * 128 + ((7 ^ (rt & 7)) << 4)) = o;
-          }
-          *reinterpret_cast<float2*>(smem + C::SC_OFF + ks * C::SC_BYTES + rt * 8) = sc_c;
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(k_full(ks));
+        if (bad) break;
         ++g;
-        base += npairs;
         if (have_n) {
           st_c = st_n;
           n_c = n_n;
-          par_c = par_n;
-          tail_c = tail_n;
-          sc_c = sc_n;
-          todd_c = todd_n;
           sl_c = sl_n;
+          sc_c = sc_n;
+          have_n = false;
           continue;
         }
         if (look == 0) break;  // the lookahead already consumed the end of the stream
         r = next_tile(true, st_c);
         if (r != 1) break;
-        take(st_c, n_c, tail_c, sc_c, todd_c, sl_c);
+        take(st_c, n_c, sl_c, sc_c);
         release();
-        par_c = 0;
-#pragma unroll 1
-        for (int j = 0; j < kPA; ++j) copy_pair(sl_c, j, base + j, par_c);
+        copy_unit(sl_c, 0);
+        copy_unit(sl_c, 1);
       }
     }
     // drain this thread's outstanding cp.async copies before the CTA can finish
