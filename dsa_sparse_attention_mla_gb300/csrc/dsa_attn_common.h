@@ -20,12 +20,14 @@ dsa_status_t encode_q_tensor_map(const dsa_attn_args_t* a, int dk, CUtensorMap* 
 int next_attn_epoch(const void* workspace);
 
 // Workspace of the split-token merge, per persistent CTA b: partial o [b][64 * 256] fp32,
-// (max, sum) [b][2][64] fp32 and eight publish flags [b][8] int32.
+// (max, sum) [b][2][64] fp32 and eight publish flags [b][8] int32; then the work-balanced split:
+// valid-entry counts of 32 unit slices per CTA and the G + 1 range bounds, int64.
 size_t attn_ws_bytes(int sm_count);
 struct AttnWorkspace {
   float* o;
   float* ml;
   int* flags;
+  int64_t* split;
 };
 AttnWorkspace attn_ws_layout(void* workspace, int sm_count);
 

@@ -61,6 +61,12 @@ __device__ __forceinline__ int loader_index(int warp) { return warp == 3 ? 0 : (
 constexpr int kMaxParts = 16;     // most parts of one split token (the launch guarantees it)
 constexpr int kRing = 8;          // ring of a packed-row loader warp: 2 units of 8 half rows (2 KB)
 constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr int kSplitMaxCtas = 192;  // most CTAs of a work-balanced split (its bounds live in shared memory)
+constexpr int kSplitSlices = 32;    // unit slices per CTA counted by the split pre-pass
+// Work of a token beyond its tiles, in key equivalents: its first tile takes the exact-maximum
+// path and its segment end the epilogue (row sums, merge, output). Clock traces of CTAs that
+// hold one-tile and sixteen-tile tokens put that at about 5.5 full tiles.
+constexpr int kSegmentWeight = 704;
 
 template <int KIND>
 struct Cfg {
@@ -85,7 +91,8 @@ struct Cfg {
   static constexpr int RED_OFF = RING_OFF + RING_BYTES;
   // m[64], alpha[64], lsum[64], spare[64], part[4][64], wk[kMaxParts][64], votes[2][8]
   static constexpr int RED_FLOATS = 8 * kH + kMaxParts * kH + 2 * kNSM;
-  static constexpr int BAR_OFF = RED_OFF + ((RED_FLOATS * 4 + 15) & ~15);
+  static constexpr int SPLIT_OFF = RED_OFF + ((RED_FLOATS * 4 + 15) & ~15);  // producer: range bounds
+  static constexpr int BAR_OFF = SPLIT_OFF + 8 * (kSplitMaxCtas + 1);
   static constexpr int NBARS = 2 + 4 * kKST + 2 * kMST + 8 + 3;
   static constexpr int MISC_OFF = BAR_OFF + 8 * NBARS;
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + alignment slack
@@ -140,6 +147,10 @@ struct Params {
   int NT;     // 128-position tiles per token (over the index width)
   int64_t U;  // total units = T * NT
   int G;      // CTAs
+  // work-balanced split (null: CTA b takes units [b U / G, (b + 1) U / G)): the first unit of
+  // each CTA's range by work, G + 1 values, and the fewest units a range may hold
+  const int64_t* bounds;
+  int split_gap;
 };
 
 __device__ __forceinline__ void set_err(int32_t* err, int bits) {
@@ -247,7 +258,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     // dropped and the valid ones packed, in index order, into dense 128-key tiles, so runs of
     // padding cost only their index reads and every emitted tile but a segment's last is full.
     uint32_t mc = 0, qc = 0;
-    const int64_t u0 = unit_begin(b, p.U, p.G), u1 = unit_begin(b + 1, p.U, p.G);
+    // range bounds of every CTA. A work-balanced split comes with a bound per CTA by valid
+    // entries; they are spaced to at least split_gap units (so that a token spans few CTAs)
+    // by a running maximum of bounds[c] - c * gap, capped at U - (G - c) * gap.
+    int64_t* sb = reinterpret_cast<int64_t*>(smem + C::SPLIT_OFF);
+    if (p.bounds) {
+      const int64_t gap = p.split_gap;
+      constexpr int kPer = (kSplitMaxCtas + 32) / 32;  // bounds per lane, in order
+      int64_t v[kPer];
+      int64_t run = INT64_MIN;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int c = kPer * lane + i;
+        v[i] = c <= p.G ? p.bounds[c] - c * gap : INT64_MIN;
+        run = v[i] > run ? v[i] : run;
+        v[i] = run;
+      }
+      int64_t pre = INT64_MIN;  // running maximum of the lanes below
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t x = __shfl_up_sync(0xffffffffu, run, o);
+        if (lane >= o) run = x > run ? x : run;
+      }
+      pre = __shfl_up_sync(0xffffffffu, run, 1);
+      if (lane == 0) pre = INT64_MIN;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int c = kPer * lane + i;
+        if (c <= p.G) {
+          const int64_t lo = (v[i] > pre ? v[i] : pre) + c * gap, hi = p.U - (int64_t)(p.G - c) * gap;
+          sb[c] = c == 0 ? 0 : (c == p.G ? p.U : (lo < hi ? lo : hi));
+        }
+      }
+      __syncwarp();
+    }
+    const int64_t u0 = p.bounds ? sb[b] : unit_begin(b, p.U, p.G);
+    const int64_t u1 = p.bounds ? sb[b + 1] : unit_begin(b + 1, p.U, p.G);
     auto emit_begin = [&](int& st) -> MetaHdr* {
       st = mc % kMST;
       if (mc >= (uint32_t)kMST) wait(m_empty(st), ((mc / kMST) & 1) ^ 1);
@@ -395,11 +441,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           me->had_tiles = had ? 1 : 0;
           int last = b;
           if (kind == kHead) {
-            // the last CTA c whose range starts at or before the token's last unit L:
-            // floor(c * U / G) <= L  <=>  c <= ceil((L + 1) * G / U) - 1
+            // the last CTA c whose range starts at or before the token's last unit L
             const int64_t L1 = (t + 1) * p.NT;
-            const int64_t c = (L1 * p.G + p.U - 1) / p.U - 1;
-            last = (int)(c < p.G - 1 ? c : p.G - 1);
+            if (p.bounds) {
+              int lo = b, hi = p.G - 1;  // sb[lo] <= L1 - 1 holds; find the largest such c
+              while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (sb[mid] <= L1 - 1) lo = mid;
+                else hi = mid - 1;
+              }
+              last = lo;
+            } else {
+              // floor(c * U / G) <= L  <=>  c <= ceil((L + 1) * G / U) - 1
+              const int64_t c = (L1 * p.G + p.U - 1) / p.U - 1;
+              last = (int)(c < p.G - 1 ? c : p.G - 1);
+            }
           }
           me->merge_last = last;
         }
@@ -1074,6 +1130,130 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ------------------------------------------------------------- work-balanced split --
+// Units (token, 128-entry window) carry very different work when the index lists are uneven
+// (causal prefill: the early tokens' windows are mostly padding). Two small kernels turn the
+// lists into per-CTA range bounds by work (non-empty tiles plus a fixed amount per token), so
+// that every CTA gets about the same work. Both read only the index lists; the bounds depend on nothing else, so a split
+// (and so the result) is the same on every call.
+
+// work of unit u (window [128 j, 128 j + 128) of token u / NT): a full tile if any entry is
+// >= 0 (a token's valid entries are packed into dense tiles, and a tile costs the same however
+// full), plus the token's fixed work on its first unit
+__device__ __forceinline__ int unit_work(const int32_t* idx, int64_t idx_stride, int topk, int NT, int64_t u, int lane) {
+  const int64_t t = u / NT;
+  const int j = (int)(u - t * NT);
+  const int32_t* row = idx + t * idx_stride;
+  bool any = false;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int e = kBN * j + 32 * k + lane;
+    any |= e < topk && row[e] >= 0;
+  }
+  return (__any_sync(0xffffffffu, any) ? kBN : 0) + (j == 0 ? kSegmentWeight : 0);
+}
+
+// warp s: work of slice s = units [s U / S, (s + 1) U / S)
+__global__ void __launch_bounds__(1024) split_count_kernel(const int32_t* __restrict__ idx, int64_t idx_stride, int topk,
+                                                           int NT, int64_t U, int S, int64_t* __restrict__ tot) {
+  const int lane = threadIdx.x & 31;
+  const int s = blockIdx.x * 32 + (threadIdx.x >> 5);
+  if (s >= S) return;
+  const int64_t u0 = (int64_t)s * U / S, u1 = (int64_t)(s + 1) * U / S;
+  int64_t c = 0;
+  for (int64_t u = u0; u < u1; ++u) c += unit_work(idx, idx_stride, topk, NT, u, lane);
+  if (lane == 0) tot[s] = c;
+}
+
+// block b: bounds[b] = the first unit u with G * (work of the units before u) >= b * W (W: all
+// the work); bounds[0] = 0, bounds[G] = U
+__global__ void __launch_bounds__(256) split_bounds_kernel(const int32_t* __restrict__ idx, int64_t idx_stride, int topk,
+                                                           int NT, int64_t U, int S, int G,
+                                                           const int64_t* __restrict__ tot, int64_t* __restrict__ bounds) {
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (b == 0 || b == G) {
+    if (tid == 0) bounds[b] = b == 0 ? 0 : U;
+    return;
+  }
+  __shared__ int64_t part[256];
+  __shared__ int64_t sel_slice, sel_base;
+  // each thread takes a run of consecutive slices; an exclusive scan of the run sums gives
+  // every slice's prefix
+  const int per = (S + 255) / 256, s0 = min(S, tid * per), s1 = min(S, s0 + per);
+  int64_t mine = 0;
+  for (int s = s0; s < s1; ++s) mine += tot[s];
+  part[tid] = mine;
+  __syncthreads();
+  if (tid == 0) {
+    int64_t run = 0;
+    for (int i = 0; i < 256; ++i) {
+      const int64_t x = part[i];
+      part[i] = run;
+      run += x;
+    }
+    sel_base = run;  // W for now
+    sel_slice = S;
+  }
+  __syncthreads();
+  const int64_t W = sel_base, target = (int64_t)b * W;
+  __syncthreads();
+  // the slice holding the crossing: the first s with G * (prefix through s) >= b W
+  {
+    int64_t pre = part[tid];
+    for (int s = s0; s < s1; ++s) {
+      const int64_t after = pre + tot[s];
+      if ((int64_t)G * after >= target) {
+        atomicMin(reinterpret_cast<unsigned long long*>(&sel_slice), (unsigned long long)s);
+        break;
+      }
+      pre = after;
+    }
+  }
+  __syncthreads();
+  const int64_t s = sel_slice;
+  if (warp != 0) return;
+  if (s >= S) {  // no crossing (W == 0): every unit counts the same
+    if (lane == 0) bounds[b] = (int64_t)b * U / G;
+    return;
+  }
+  // prefix before slice s, then walk its units
+  int64_t cum = 0;
+  {
+    const int per_s = (S + 31) / 32;
+    for (int i = lane * per_s; i < min(S, (lane + 1) * per_s) && i < s; ++i) cum += tot[i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cum += __shfl_xor_sync(0xffffffffu, cum, o);
+  }
+  const int64_t u0 = s * U / S, u1 = (s + 1) * U / S;
+  int64_t bound = u1;
+  for (int64_t ub = u0; ub < u1; ub += 32) {  // 32 units a round, one per lane
+    const int64_t u = ub + lane;
+    int c = 0;
+    if (u < u1) {
+      const int64_t t = u / NT;
+      const int j = (int)(u - t * NT);
+      const int32_t* row = idx + t * idx_stride;
+      const int e1 = min(topk, kBN * (j + 1));
+      bool any = false;
+      for (int e = kBN * j; e < e1 && !any; ++e) any = row[e] >= 0;
+      c = (any ? kBN : 0) + (j == 0 ? kSegmentWeight : 0);
+    }
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += x;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, u < u1 && (int64_t)G * (cum + incl - c) >= target);
+    if (hit) {
+      bound = ub + __ffs(hit) - 1;
+      break;
+    }
+    cum += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) bounds[b] = bound;
+}
+
 template <int KIND>
 static dsa_status_t launch(const dsa_attn_args_t* a, const DeviceInfo& dev, cudaStream_t stream) {
   using C = Cfg<KIND>;
@@ -1131,6 +1311,23 @@ static dsa_status_t launch(const dsa_attn_args_t* a, const DeviceInfo& dev, cuda
     --G;
   }
   p.G = (int)G;
+  // Work-balanced split when CTAs hold many units (long, possibly uneven index lists): two small
+  // kernels on the same stream turn the lists into range bounds by work. Ranges keep at
+  // least ceil(NT / (kMaxParts - 1)) units, so that a token still spans at most kMaxParts CTAs.
+  p.bounds = nullptr;
+  p.split_gap = 1;
+  const int64_t gap = (p.NT + kMaxParts - 2) / (kMaxParts - 1);
+  if (p.G > 1 && p.G <= kSplitMaxCtas && p.U / p.G >= 64 && p.U >= (int64_t)p.G * gap) {
+    const int S = kSplitSlices * p.G;
+    int64_t* tot = ws.split;
+    int64_t* bnd = ws.split + S;
+    split_count_kernel<<<p.G, 1024, 0, stream>>>(p.idx, p.idx_stride, p.topk, p.NT, p.U, S, tot);
+    split_bounds_kernel<<<p.G + 1, 256, 0, stream>>>(p.idx, p.idx_stride, p.topk, p.NT, p.U, S, p.G, tot, bnd);
+    const cudaError_t le = cudaGetLastError();
+    if (le != cudaSuccess) return cuda_fail(le);
+    p.bounds = bnd;
+    p.split_gap = (int)gap;
+  }
 
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)p.G);

@@ -246,3 +246,18 @@ def test_fp8_tile_scales_applied_per_tile(gpu, e):
     undo = np.concatenate([np.full(128, 2.0 ** e), np.full(128, 2.0 ** -e)])
     check_close(f32_of(out) * undo, ref * undo, "fp8 tile scales")
     _check_lse(f32_of(lse_t), ref_lse, 2e-4)
+
+
+def test_balanced_split_causal_prefill(gpu):
+    """Long causal lists (T=3072, top-k 2048): every CTA holds hundreds of (token, 128-entry)
+    units, so the CTA ranges come from the work-balanced split by valid entries, and the first
+    2048 tokens' lists are mostly padding. Sampled tokens (including split ones) against the
+    oracle; repeated calls are bit-identical (the split depends only on the index lists)."""
+    wl = W.prefill_causal(T=3072, topk=2048, window=128, seed=31, name="prefill_causal_T3072")
+    rng = np.random.default_rng(5)
+    tokens = np.unique(np.concatenate([np.arange(0, wl.T, 97), rng.integers(0, wl.T, 16),
+                                       [0, 1, 127, 128, 2047, 2048, wl.T - 1]]))
+    out = _check(wl, gpu, tokens=tokens)
+    cache = oracle_cache(wl)
+    again, _ = _gpu_attn(wl, cache, gpu)
+    assert torch.equal(again.view(torch.int16), out.view(torch.int16))
