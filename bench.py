@@ -66,6 +66,21 @@ def _recorded_traffic(workload):
     return None if w is None else int(w["traffic"])
 
 
+def kernels_per_call(wl, sm_count):
+    """Kernel launches of one dsa_sparse_attn call, by the launcher's own rule: the 256+0 kernel
+    (d_nope 256, no rope) takes a work-balanced split, two small pre-pass kernels, when its
+    CTAs hold at least 64 (token, 128-entry) units each; every other call is one launch."""
+    if wl.d_nope != 256 or wl.d_rope != 0:
+        return 1
+    nt = (wl.indices.shape[1] + 127) // 128
+    u = wl.T * nt
+    g = min(sm_count, (u + 3) // 4)
+    while g > 1 and (nt + u // g - 1) // (u // g) + 1 > 17:
+        g -= 1
+    gap = (nt + 14) // 15
+    return 3 if (1 < g <= 192 and u // g >= 64 and u >= g * gap) else 1
+
+
 def algorithmic_work(wl):
     """Algorithmic bytes and FLOPs of one full call (per the data each token must touch once):
     gathered rows (valid entries x row bytes) + q + out + the index list + the block table;
@@ -374,7 +389,7 @@ def main():
         "cpu_baseline": {"value": cpu_v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": world * wl.T / (r["e2e_ms"] / 1000.0), "unit": "tokens/s", "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"]},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * kernels_per_call(wl, torch.cuda.get_device_properties(device).multi_processor_count),
         "clocks": r["clocks"],
         "step_ms": {"median": statistics.median(r["times"]), "min": min(r["times"]), "max": max(r["times"])},
     }

@@ -35,3 +35,11 @@ def test_recorded_traffic_tracks_kernel_sources(tmp_path, monkeypatch):
     assert bench._recorded_traffic("other") is None
     (src / "k.cu").write_text("kernel v2")
     assert bench._recorded_traffic("w") is None
+
+
+def test_kernels_per_call_follows_the_launch_rule():
+    # decode T=256 x 17 windows on 152 SMs: 28 units per CTA, one launch; causal prefill
+    # T=8192 x 16 windows: 862 units per CTA, split pre-pass + attention; 512+64: one launch
+    assert bench.kernels_per_call(W.config(3), 152) == 1
+    assert bench.kernels_per_call(W.config(4), 152) == 3
+    assert bench.kernels_per_call(W.config(5), 152) == 1
