@@ -28,9 +28,10 @@
 //    contiguous ranges per CTA; a token cut by a range boundary is merged in-kernel by the CTA
 //    holding its first tiles (fixed order, no atomics on data).
 //  * Warp roles: 0 producer (index read, -1 compaction into dense 128-key tiles, page
-//    translation, L2 prefetch of packed rows, Q loads by TMA), 1 score-MMA issuer, 2 output-MMA
-//    issuer, 4-7 softmax and epilogue, 8-15 row loaders (cp.async copies of bf16 rows, or loads
-//    of packed rows widened into the 128-byte-swizzled K tile); warp 3 idle.
+//    translation, Q loads by TMA), 1 score-MMA issuer, 2 output-MMA issuer, 4-7 softmax and
+//    epilogue, 3 and 8-15 row loaders (cp.async copies of bf16 rows straight into the tile, or
+//    of packed half rows into a ring, widened into the 128-byte-swizzled K tile). Packed rows
+//    are not prefetched into L2: the extra whole-line traffic cost more than it saved.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -400,15 +401,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool ok = slot >= 0;
           const uint32_t bal = __ballot_sync(0xffffffffu, ok);
           if (ok) cbuf[nstep + __popc(bal & ((1u << lane) - 1u))] = (int)slot;
-          if constexpr (C::FP8) {
-            // pull the packed row into L2 a few tiles before the loaders read it (one LSU
-            // prefetch per 128-byte line it touches)
-            if (ok) {
-              const uintptr_t r0 = reinterpret_cast<uintptr_t>(p.cache + slot * C::RB);
-              for (uintptr_t a = r0 & ~uintptr_t(127); a < r0 + C::RB; a += 128)
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(a > r0 ? a : r0));
-            }
-          }
           nstep += __popc(bal);
         }
         if (bad) set_err(p.err, DSA_DEVERR_INDEX_OUT_OF_RANGE);
