@@ -761,10 +761,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
       }
       const uint32_t lfin = tl + C::L_COL + 64 * lb + hb;  // the buffer the last pass wrote
-      // row sums: each lane's partial sums of its 32 heads go to its row of a [128][64] fp32
-      // block in the (idle) P buffers, 16-byte granule q of row r at ((q ^ (r & 15)) << 4); then
-      // thread h < 64 adds up column h (a warp reads 32 consecutive columns of one row)
-      float* lrow = reinterpret_cast<float*>(smem + C::P_OFF);
+      // row sums: per warp, a reduce-scatter over the lanes (keys) of each 16-head chunk leaves
+      // the warp's sum of head 16 ch + (lane >> 1) in lanes 2i and 2i + 1 (each round halves the
+      // values a lane holds: it keeps one half, adds its partner's copy of that half, and hands
+      // over the other); lane 2i writes it to red_part[quarter][head], and thread h < 64 adds
+      // up the quarters
 #pragma unroll 1
       for (int ch = 0; ch < kCH; ++ch) {
         uint32_t l[16];
@@ -775,25 +776,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) l[i] = 0u;
         }
+        float v8[8], v4[4], v2[2];
+        const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int gq = (hb >> 2) + 4 * ch + q;
-          *reinterpret_cast<uint4*>(lrow + tr * kH + ((gq ^ (tr & 15)) << 2)) =
-              make_uint4(l[4 * q], l[4 * q + 1], l[4 * q + 2], l[4 * q + 3]);
+        for (int i = 0; i < 8; ++i) {
+          const float lo = u2f(l[i]), hi = u2f(l[i + 8]);
+          v8[i] = (b4 ? hi : lo) + __shfl_xor_sync(0xffffffffu, b4 ? lo : hi, 16);
         }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v4[i] = (b3 ? v8[i + 4] : v8[i]) + __shfl_xor_sync(0xffffffffu, b3 ? v8[i] : v8[i + 4], 8);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) v2[i] = (b2 ? v4[i + 2] : v4[i]) + __shfl_xor_sync(0xffffffffu, b2 ? v4[i] : v4[i + 2], 4);
+        float v1 = (b1 ? v2[1] : v2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? v2[0] : v2[1], 2);
+        v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+        if ((lane & 1) == 0) red_part[qd * 64 + hb + 16 * ch + (lane >> 1)] = v1;
       }
       if (xsync(false) < 0) break;
       float lsum = 0.0f, mrow = -INFINITY;
-      if (sid < kH) {
-        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll 4
-        for (int r = 0; r < kBN; ++r) acc[r & 3] += lrow[r * kH + ((((sid >> 2) ^ (r & 15))) << 2) + (sid & 3)];
-        if (had) {
-          lsum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-          mrow = red_m[sid];
-        }
+      if (sid < kH && had) {
+        lsum = (red_part[sid] + red_part[64 + sid]) + (red_part[128 + sid] + red_part[192 + sid]);
+        mrow = red_m[sid];
       }
-      if (xsync(false) < 0) break;  // the block is read before anyone reuses the P buffers
+      if (xsync(false) < 0) break;  // the quarter sums are read before a next tile reuses them
       if (kind == kPart) {
         // publish (O^T, m, l) of this part in workspace slot b
         if (sid < kH) {
