@@ -830,18 +830,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       // complete token, or the head of a split token: merge parts b+1 .. last in order
       const int nparts = kind == kHead ? last - b : 0;
       bool okp = true;
-      for (int k = 1; k <= nparts && okp; ++k) {
-        for (int j = 0; j < kNSM && okp; ++j) {
-          int v = 0;
-          const uint64_t t0 = globaltimer_ns();
-          for (;;) {
-            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p.flags + 8 * (b + k) + j) : "memory");
-            if (v == p.epoch || globaltimer_ns() - t0 > kWaitNs) break;
-            __nanosleep(64);
+      // every publish flag of parts b+1 .. last, one per lane (a warp vote ends the wait); the
+      // warp barrier then orders every lane's reads of the parts after the acquiring loads
+      for (int f0 = 0; f0 < nparts * kNSM && okp; f0 += 32) {
+        const int f = f0 + lane;
+        const bool mine = f < nparts * kNSM;
+        const int* fp = p.flags + 8 * (b + 1 + f / kNSM) + f % kNSM;
+        const uint64_t t0 = globaltimer_ns();
+        for (;;) {
+          int v = p.epoch;
+          if (mine) asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(fp) : "memory");
+          if (__all_sync(0xffffffffu, v == p.epoch)) break;
+          if (__any_sync(0xffffffffu, globaltimer_ns() - t0 > kWaitNs)) {
+            okp = false;
+            break;
           }
-          okp = v == p.epoch;
+          __nanosleep(64);
         }
       }
+      __syncwarp();
       if (!okp) fail(DSA_DEVERR_TIMEOUT);
       // (the launch keeps nparts <= kMaxParts; more would overrun the weight table)
       const int np = (okp && nparts <= kMaxParts) ? nparts : 0;
