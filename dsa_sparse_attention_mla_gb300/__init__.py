@@ -21,7 +21,7 @@ import threading
 __all__ = [
     "DsaError", "CACHE_BF16", "CACHE_FP8_SCALED", "DEVERR_INDEX_OUT_OF_RANGE", "DEVERR_TIMEOUT",
     "DEVERR_SLOT_OUT_OF_RANGE", "library_path", "load_library", "dsa_status_string",
-    "dsa_packed_row_bytes", "dsa_cache_row_bytes", "dsa_quant_k_cache", "dsa_gather_dequant",
+    "dsa_packed_row_bytes", "dsa_cache_row_bytes", "dsa_quant_k_cache", "dsa_gather_dequant", "dsa_gather_requant",
     "dsa_sparse_attn_workspace_size", "dsa_sparse_attn", "dsa_sparse_attn_static_ws", "DsaAttnArgs",
 ]
 
@@ -87,6 +87,8 @@ def load_library():
         lib.dsa_quant_k_cache.restype = i32
         lib.dsa_gather_dequant.argtypes = [P, i32, i64, i32, i32, P, i64, P, i64, i32, i32, P, P, P, P]
         lib.dsa_gather_dequant.restype = i32
+        lib.dsa_gather_requant.argtypes = [P, i64, i32, i32, P, i64, P, i64, i32, i32, P, P, P, i64, P, P]
+        lib.dsa_gather_requant.restype = i32
         lib.dsa_sparse_attn_workspace_size.argtypes = [ctypes.POINTER(DsaAttnArgs), ctypes.POINTER(ctypes.c_size_t)]
         lib.dsa_sparse_attn_workspace_size.restype = i32
         lib.dsa_sparse_attn.argtypes = [ctypes.POINTER(DsaAttnArgs), P]
@@ -185,6 +187,34 @@ def dsa_gather_dequant(cache, kind: int, d_nope: int, d_rope: int, indices, *, b
         max_pages, _ptr(None if req_of_index is None else req_of_index.contiguous()), _ptr(out), _ptr(error_word),
         _stream(indices.device))
     _check(st, "dsa_gather_dequant")
+    return out
+
+
+def dsa_gather_requant(cache, d_nope: int, d_rope: int, indices, *, block_table=None, page_size=0,
+                       req_of_index=None, out_loc=None, out=None, out_slots=None, error_word=None):
+    """Packed rows gathered by index and packed again (uint8 [n, row_bytes], or written into
+    rows out_loc of ``out``)."""
+    import torch
+
+    _need_cuda("cache", cache, torch.uint8)
+    _need_cuda("indices", indices, torch.int32)
+    _need_cuda("block_table", block_table, torch.int32)
+    _need_cuda("req_of_index", req_of_index, torch.int32)
+    _need_cuda("out_loc", out_loc, torch.int64)
+    indices = indices.contiguous().view(-1)
+    n = indices.numel()
+    rb = dsa_packed_row_bytes(d_nope, d_rope)
+    if out is None:
+        out = torch.empty((n if out_loc is None else int(out_slots), rb), dtype=torch.uint8, device=indices.device)
+    _need_cuda("out", out, torch.uint8)
+    bt_stride = 0 if block_table is None else block_table.stride(0)
+    max_pages = 0 if block_table is None else block_table.shape[1]
+    st = load_library().dsa_gather_requant(
+        _ptr(cache), cache.shape[0], d_nope, d_rope, _ptr(indices), n, _ptr(block_table), bt_stride, page_size,
+        max_pages, _ptr(None if req_of_index is None else req_of_index.contiguous()),
+        _ptr(None if out_loc is None else out_loc.contiguous()), _ptr(out), out.shape[0], _ptr(error_word),
+        _stream(indices.device))
+    _check(st, "dsa_gather_requant")
     return out
 
 

@@ -57,6 +57,26 @@ dsa_status_t current_device(DeviceInfo* out) {
 }
 
 // ----------------------------------------------------------------------------- pack kernel --
+// Packs one 128-element tile held by a warp, lane l owning elements 4 l .. 4 l + 3 (x):
+// amax over the tile, scale = amax / 448, codes = e4m3_rne_satfinite(x / scale) (IEEE divisions;
+// an all-zero tile stores scale 0 and codes 0). Writes lane l's four codes to codes + 4 l and the
+// scale (lane 0) to *scale_out.
+__device__ __forceinline__ void pack_tile(const float (&x)[4], int lane, uint8_t* codes_out, float* scale_out) {
+  float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  uint32_t codes = 0;
+  float scale = 0.0f;
+  if (amax > 0.0f) {
+    scale = __fdiv_rn(amax, 448.0f);
+    const uint16_t c01 = f32x2_to_e4m3x2(__fdiv_rn(x[0], scale), __fdiv_rn(x[1], scale));
+    const uint16_t c23 = f32x2_to_e4m3x2(__fdiv_rn(x[2], scale), __fdiv_rn(x[3], scale));
+    codes = (uint32_t)c01 | ((uint32_t)c23 << 16);
+  }
+  *reinterpret_cast<uint32_t*>(codes_out + 4 * lane) = codes;
+  if (lane == 0) *scale_out = scale;
+}
+
 // One warp per row. For tile j, lane l owns elements [128 j + 4 l, 128 j + 4 l + 4).
 template <int D_NOPE, int D_ROPE>
 __global__ void __launch_bounds__(256) quant_k_cache_kernel(const uint16_t* __restrict__ k_nope, int64_t nope_stride,
@@ -84,19 +104,7 @@ __global__ void __launch_bounds__(256) quant_k_cache_kernel(const uint16_t* __re
     x[1] = __uint_as_float(raw.x & 0xFFFF0000u);
     x[2] = __uint_as_float(raw.y << 16);
     x[3] = __uint_as_float(raw.y & 0xFFFF0000u);
-    float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    uint32_t codes = 0;
-    float scale = 0.0f;
-    if (amax > 0.0f) {
-      scale = __fdiv_rn(amax, 448.0f);
-      const uint16_t c01 = f32x2_to_e4m3x2(__fdiv_rn(x[0], scale), __fdiv_rn(x[1], scale));
-      const uint16_t c23 = f32x2_to_e4m3x2(__fdiv_rn(x[2], scale), __fdiv_rn(x[3], scale));
-      codes = (uint32_t)c01 | ((uint32_t)c23 << 16);
-    }
-    *reinterpret_cast<uint32_t*>(dst + 128 * j + 4 * lane) = codes;
-    if (lane == 0) *reinterpret_cast<float*>(dst + D_NOPE + 4 * j) = scale;
+    pack_tile(x, lane, dst + 128 * j, reinterpret_cast<float*>(dst + D_NOPE + 4 * j));
   }
   if constexpr (D_ROPE > 0) {
     // D_ROPE bf16 = 2*D_ROPE bytes copied as 4-byte words (the RoPE part starts 8-byte aligned)
@@ -168,6 +176,58 @@ __global__ void __launch_bounds__(256) gather_dequant_kernel(const uint8_t* __re
       uint32_t* rd = reinterpret_cast<uint32_t*>(o + D_NOPE);
       for (int w = lane; w < D_ROPE / 2; w += 32) rd[w] = rs[w];
     }
+  }
+}
+
+// ----------------------------------------------------------------- gather / requant kernel --
+// One warp per row: gather packed row indices[i] (direct or paged, as gather_dequant), widen each
+// tile to bf16_rne(fp32(e4m3(code)) * scale) exactly as gather_dequant does, and pack those
+// values again (pack_tile) into row out_loc[i] (or i) of `out`; RoPE bits are copied. A masked
+// index, or one that addresses no slot, packs the zero row.
+template <int D_NOPE, int D_ROPE>
+__global__ void __launch_bounds__(256) gather_requant_kernel(const uint8_t* __restrict__ cache, int64_t num_slots,
+                                                             const int32_t* __restrict__ indices, int64_t n,
+                                                             const int32_t* __restrict__ bt, int64_t bt_stride,
+                                                             int page_size, int max_pages,
+                                                             const int32_t* __restrict__ req_of_index,
+                                                             const int64_t* __restrict__ out_loc, uint8_t* __restrict__ out,
+                                                             int64_t out_slots, int32_t* error_word) {
+  constexpr int TILES = D_NOPE / 128;
+  constexpr int64_t RB = D_NOPE + 4 * TILES + 2 * D_ROPE;
+  const int lane = threadIdx.x & 31;
+  const int64_t i = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (i >= n) return;
+  const int64_t dslot = out_loc ? out_loc[i] : i;
+  if (dslot < 0 || dslot >= out_slots) {
+    if (lane == 0 && error_word) atomicOr(error_word, DSA_DEVERR_SLOT_OUT_OF_RANGE);
+    return;
+  }
+  const int64_t req = req_of_index ? req_of_index[i] : 0;
+  const int64_t slot = translate_slot(indices[i], req, num_slots, bt, bt_stride, page_size, max_pages);
+  if (slot == -2 && lane == 0 && error_word) atomicOr(error_word, DSA_DEVERR_INDEX_OUT_OF_RANGE);
+  const uint8_t* r = slot >= 0 ? cache + slot * RB : nullptr;
+  uint8_t* dst = out + dslot * RB;
+#pragma unroll
+  for (int j = 0; j < TILES; ++j) {
+    float x[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (r) {
+      const uint32_t c = *reinterpret_cast<const uint32_t*>(r + 128 * j + 4 * lane);
+      const float sc = *reinterpret_cast<const float*>(r + D_NOPE + 4 * j);
+      const float2 a = f16x2_to_f32x2(e4m3x2_to_f16x2((uint16_t)(c & 0xFFFFu)));
+      const float2 b = f16x2_to_f32x2(e4m3x2_to_f16x2((uint16_t)(c >> 16)));
+      const uint32_t w0 = f32x2_to_bf16x2(__fmul_rn(a.x, sc), __fmul_rn(a.y, sc));
+      const uint32_t w1 = f32x2_to_bf16x2(__fmul_rn(b.x, sc), __fmul_rn(b.y, sc));
+      x[0] = __uint_as_float(w0 << 16);
+      x[1] = __uint_as_float(w0 & 0xFFFF0000u);
+      x[2] = __uint_as_float(w1 << 16);
+      x[3] = __uint_as_float(w1 & 0xFFFF0000u);
+    }
+    pack_tile(x, lane, dst + 128 * j, reinterpret_cast<float*>(dst + D_NOPE + 4 * j));
+  }
+  if constexpr (D_ROPE > 0) {
+    uint32_t* rd = reinterpret_cast<uint32_t*>(dst + D_NOPE + 4 * TILES);
+    const uint32_t* rs = r ? reinterpret_cast<const uint32_t*>(r + D_NOPE + 4 * TILES) : nullptr;
+    for (int w = lane; w < D_ROPE / 2; w += 32) rd[w] = rs ? rs[w] : 0u;
   }
 }
 
@@ -260,6 +320,36 @@ dsa_status_t dsa_gather_dequant(const void* cache, dsa_cache_kind_t kind, int64_
     if (d_nope == 256) DSA_GD(DSA_CACHE_FP8_SCALED, 256, 0); else DSA_GD(DSA_CACHE_FP8_SCALED, 512, 64);
   }
 #undef DSA_GD
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? DSA_OK : cuda_fail(e);
+}
+
+dsa_status_t dsa_gather_requant(const void* cache, int64_t num_slots, int d_nope, int d_rope, const int32_t* indices,
+                                int64_t n, const int32_t* block_table, int64_t bt_stride, int page_size, int max_pages,
+                                const int32_t* req_of_index, const int64_t* out_loc, void* out, int64_t out_slots,
+                                int32_t* error_word, void* stream) {
+  if (n < 0 || num_slots < 0 || out_slots < 0) return DSA_ERR_INVALID_ARGUMENT;
+  if (!((d_nope == 256 && d_rope == 0) || (d_nope == 512 && d_rope == 64)))
+    return (d_nope > 0 && d_nope % 128 == 0 && d_rope >= 0) ? DSA_ERR_UNSUPPORTED : DSA_ERR_INVALID_ARGUMENT;
+  if (n == 0) return DSA_OK;
+  if (!cache || !indices || !out) return DSA_ERR_INVALID_ARGUMENT;
+  if (!aligned(cache, 8) || !aligned(out, 8)) return DSA_ERR_INVALID_ARGUMENT;
+  if (!out_loc && n > out_slots) return DSA_ERR_INVALID_ARGUMENT;
+  if (block_table && (page_size <= 0 || max_pages <= 0 || bt_stride < max_pages)) return DSA_ERR_INVALID_ARGUMENT;
+  DeviceInfo dev;
+  dsa_status_t st = current_device(&dev);
+  if (st != DSA_OK) return st;
+  const dim3 block(256);
+  const dim3 grid((unsigned)((n + 7) / 8));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint8_t* c = static_cast<const uint8_t*>(cache);
+  uint8_t* o = static_cast<uint8_t*>(out);
+  if (d_nope == 256)
+    gather_requant_kernel<256, 0><<<grid, block, 0, s>>>(c, num_slots, indices, n, block_table, bt_stride, page_size,
+                                                         max_pages, req_of_index, out_loc, o, out_slots, error_word);
+  else
+    gather_requant_kernel<512, 64><<<grid, block, 0, s>>>(c, num_slots, indices, n, block_table, bt_stride, page_size,
+                                                          max_pages, req_of_index, out_loc, o, out_slots, error_word);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? DSA_OK : cuda_fail(e);
 }

@@ -111,6 +111,27 @@ DSA_API dsa_status_t dsa_gather_dequant(const void* cache, dsa_cache_kind_t kind
                                 int max_pages, const int32_t* req_of_index, void* out,
                                 int32_t* error_word, void* stream);
 
+/*
+ * dsa_gather_requant - gather packed scaled-FP8 rows by index and pack them again
+ * (dequant_k_cache: the gather/dequant/requant path; PR #38547, its production-file list). Row i
+ * of the result is exactly dsa_quant_k_cache applied to the bf16 row dsa_gather_dequant returns
+ * for indices[i]: each gathered tile is widened to bf16_rne(fp32(e4m3(code)) * scale), then
+ * re-packed (new amax, scale = amax / 448, codes = e4m3_rne_satfinite(x / scale)); RoPE bits are
+ * copied. A masked index (< 0), or one that addresses no slot (which also sets
+ * DSA_DEVERR_INDEX_OUT_OF_RANGE), packs the all-zero row.
+ *   cache         uint8 [num_slots, row_bytes] packed rows (8-byte aligned base)
+ *   indices, block_table, bt_stride, page_size, max_pages, req_of_index: as for dsa_gather_dequant
+ *   out_loc       int64 [n] destination row of each result in `out`, or NULL (row i); a row
+ *                 outside [0, out_slots) is skipped and sets DSA_DEVERR_SLOT_OUT_OF_RANGE
+ *   out           uint8 [out_slots, row_bytes] (8-byte aligned base); may not overlap `cache`
+ * Supported: d_nope in {256, 512}, d_rope in {0, 64}. n == 0 is a no-op.
+ */
+DSA_API dsa_status_t dsa_gather_requant(const void* cache, int64_t num_slots, int d_nope, int d_rope,
+                                const int32_t* indices, int64_t n, const int32_t* block_table,
+                                int64_t bt_stride, int page_size, int max_pages,
+                                const int32_t* req_of_index, const int64_t* out_loc, void* out,
+                                int64_t out_slots, int32_t* error_word, void* stream);
+
 /* Arguments of dsa_sparse_attn. Zero-initialise, then fill. */
 typedef struct dsa_attn_args {
   const void* q;                 /* bf16 [T, H, d_nope + d_rope]; element (t,h,d) at

@@ -161,6 +161,26 @@ def gather_dequant(cache, kind: int, d_nope: int, d_rope: int, indices, *, block
     return out, int(bad)
 
 
+# ------------------------------------------------------------------------- gather/requant --
+def gather_requant(cache, d_nope: int, d_rope: int, indices, *, block_table=None, page_size: int = 0,
+                   req_of_index=None, out_loc=None, out=None, out_slots=None):
+    """Packed rows gathered by index and packed again: by definition the pack of the bf16 rows the
+    gather/dequant path returns (PR #38547, production-file list: dequant_k_cache's direct, paged
+    and gather/dequant/requant paths). A masked or out-of-range index gives the zero row, whose
+    pack is all-zero codes and scales.
+
+    Returns (uint8 [n or out_slots, row_bytes], number of indices that addressed no slot)."""
+    deq, bad = gather_dequant(cache, CACHE_FP8_SCALED, d_nope, d_rope, indices, block_table=block_table,
+                              page_size=page_size, req_of_index=req_of_index)
+    n = deq.shape[0]
+    if out is None:
+        out_slots = n if out_loc is None else int(out_slots)
+        out = np.zeros((out_slots, packed_row_bytes(d_nope, d_rope)), dtype=np.uint8)
+    out = quant_k_cache(deq[:, :d_nope], deq[:, d_nope:] if d_rope else None, out_loc=out_loc, cache=out,
+                        num_slots=out.shape[0])
+    return out, bad
+
+
 # ----------------------------------------------------------------------------------- attention --
 def sparse_attn(q_bits, cache, kind: int, d_nope: int, d_rope: int, d_v: int, indices, sm_scale: float,
                 *, block_table=None, page_size: int = 0, req_of_token=None, tokens=None,

@@ -20,7 +20,7 @@ def _declared():
 
 def test_header_declares_the_entry_points():
     names = _declared()
-    for n in ["dsa_quant_k_cache", "dsa_gather_dequant", "dsa_sparse_attn", "dsa_sparse_attn_workspace_size",
+    for n in ["dsa_quant_k_cache", "dsa_gather_dequant", "dsa_gather_requant", "dsa_sparse_attn", "dsa_sparse_attn_workspace_size",
               "dsa_packed_row_bytes", "dsa_cache_row_bytes", "dsa_status_string", "dsa_last_cuda_error"]:
         assert n in names
 
@@ -70,6 +70,15 @@ def test_argument_errors_need_no_gpu(dsa_lib):
     assert L.dsa_quant_k_cache(fake, 256, None, 0, 0, 256, 0, None, fake, 10, None, None) == 0
     assert L.dsa_gather_dequant(fake, 7, 10, 256, 0, fake, 4, None, 0, 0, 0, None, fake, None, None) == 1
     assert L.dsa_gather_dequant(fake, 1, 10, 128, 0, fake, 4, None, 0, 0, 0, None, fake, None, None) == 2
+    i64 = ctypes.c_int64
+    assert L.dsa_gather_requant(fake, i64(10), 256, 0, fake, i64(-1), None, i64(0), 0, 0, None, None, fake, i64(10),
+                                None, None) == 1
+    assert L.dsa_gather_requant(fake, i64(10), 384, 0, fake, i64(4), None, i64(0), 0, 0, None, None, fake, i64(10),
+                                None, None) == 2
+    assert L.dsa_gather_requant(fake, i64(10), 256, 0, fake, i64(4), None, i64(0), 0, 0, None, None, fake, i64(2),
+                                None, None) == 1  # more results than output rows, no out_loc
+    assert L.dsa_gather_requant(fake, i64(10), 256, 0, fake, i64(0), None, i64(0), 0, 0, None, None, fake, i64(10),
+                                None, None) == 0
     a = dsa.DsaAttnArgs()
     a.H, a.d_nope, a.d_rope, a.d_v, a.topk, a.T = 64, 256, 0, 256, 2048, 4
     a.q = a.cache = a.indices = a.out = a.workspace = 0x10000

@@ -133,3 +133,54 @@ def test_pack_then_gather_round_trip_on_gpu_matches_oracle(gpu):
         c = dsa.dsa_quant_k_cache(bf16_dev(rows[:, :d_nope], gpu), bf16_dev(rows[:, d_nope:], gpu) if d_rope else None)
         got = dsa.dsa_gather_dequant(c, 1, d_nope, d_rope, torch.from_numpy(idx).to(gpu))
         assert np.array_equal(bits_of(got), ref)
+
+
+# ------------------------------------------------------------------------- gather / requant --
+@pytest.mark.parametrize("d_nope,d_rope", [(256, 0), (512, 64)])
+def test_gather_requant_bit_exact(gpu, d_nope, d_rope):
+    """dsa_gather_requant == the oracle's pack of its gathered bf16 rows, byte for byte; masked
+    entries pack the zero row (special rows: zero, -0, huge, constant and tiny tiles)."""
+    n = 3000
+    rows = _special_rows(n, d_nope + d_rope, seed=21)
+    cache = oracle.quant_k_cache(rows[:, :d_nope], rows[:, d_nope:] if d_rope else None)
+    rng = np.random.default_rng(4)
+    idx = rng.integers(-2, n, size=4097).astype(np.int32)
+    idx[:5] = [0, 1, 2, 3, 4]
+    ref, bad = oracle.gather_requant(cache, d_nope, d_rope, idx)
+    assert bad == 0
+    got = dsa.dsa_gather_requant(torch.from_numpy(cache).to(gpu), d_nope, d_rope, torch.from_numpy(idx).to(gpu))
+    assert np.array_equal(got.cpu().numpy(), ref)
+
+
+def test_gather_requant_paged_scatter_and_errors(gpu):
+    d_nope, d_rope, ps, pages = 512, 64, 64, 30
+    slots = ps * pages
+    rows = W.NormalRows(23, 2, slots, d_nope + d_rope).bits()
+    cache = oracle.quant_k_cache(rows[:, :d_nope], rows[:, d_nope:])
+    rng = np.random.default_rng(6)
+    bt = rng.integers(0, pages, size=(2, 10)).astype(np.int32)
+    idx = rng.integers(-1, 10 * ps, size=900).astype(np.int32)
+    idx[7] = 10 * ps + 3                                             # past the request's pages
+    req = rng.integers(0, 2, size=900).astype(np.int32)
+    out_slots = 1200
+    loc = rng.permutation(out_slots)[:900].astype(np.int64)
+    base = np.full((out_slots, cache.shape[1]), 0x5A, dtype=np.uint8)
+    ref, bad = oracle.gather_requant(cache, d_nope, d_rope, idx, block_table=bt, page_size=ps, req_of_index=req,
+                                     out_loc=loc, out=base.copy())
+    assert bad == 1
+    err = torch.zeros(1, dtype=torch.int32, device=gpu)
+    out = torch.from_numpy(base.copy()).to(gpu)
+    dsa.dsa_gather_requant(torch.from_numpy(cache).to(gpu), d_nope, d_rope, torch.from_numpy(idx).to(gpu),
+                           block_table=torch.from_numpy(bt).to(gpu), page_size=ps,
+                           req_of_index=torch.from_numpy(req).to(gpu), out_loc=torch.from_numpy(loc).to(gpu),
+                           out=out, error_word=err)
+    assert np.array_equal(out.cpu().numpy(), ref)
+    assert err.item() & dsa.DEVERR_INDEX_OUT_OF_RANGE
+    # a destination row outside the output is skipped and flagged
+    err.zero_()
+    bad_loc = torch.tensor([0, out_slots], dtype=torch.int64, device=gpu)
+    dsa.dsa_gather_requant(torch.from_numpy(cache).to(gpu), d_nope, d_rope,
+                           torch.tensor([1, 2], dtype=torch.int32, device=gpu), block_table=None,
+                           out_loc=bad_loc, out=out, error_word=err)
+    torch.cuda.synchronize()
+    assert err.item() & dsa.DEVERR_SLOT_OUT_OF_RANGE
