@@ -259,6 +259,82 @@ def run_gpu(args, wl, rank, world, device):
             "h2d": h2d, "d2h": d2h}
 
 
+def run_requant(args, device):
+    """Timing of dsa_gather_requant on the decode workload's gathered rows: every valid entry of
+    the 256 tokens (paged, 524,288 rows of 264 bytes) gathered, widened and re-packed into a
+    contiguous buffer. One JSON line like the attention bench's, HBM-bound."""
+    import torch
+
+    import dsa_sparse_attention_mla_gb300 as dsa
+    from dsa_sparse_attention_mla_gb300 import workloads as W
+
+    wl = W.config(3, seed=0)
+    _, cache, _, bt, _ = build_device_inputs(wl, device)
+    valid = wl.indices >= 0
+    pos = torch.from_numpy(wl.indices[valid].astype(np.int32)).to(device)
+    req = torch.from_numpy(np.broadcast_to(wl.req_of_token[:, None], wl.indices.shape)[valid].astype(np.int32)).to(device)
+    n = int(pos.numel())
+    rb = dsa.dsa_packed_row_bytes(wl.d_nope, wl.d_rope)
+    out = torch.empty((n, rb), dtype=torch.uint8, device=device)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        dsa.dsa_gather_requant(cache, wl.d_nope, wl.d_rope, pos, block_table=bt, page_size=wl.page_size,
+                               req_of_index=req, out=out, error_word=err)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize(device)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(device) as clk:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(device)
+    times = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    if err.item() != 0:
+        raise RuntimeError(f"device error word {err.item()} during the benchmark")
+    ms = float(sum(times)) / args.steps
+    nbytes = n * (2 * rb + 4 + 4)  # row read + row written + logical position + request
+    hbm = _peaks()[0]
+    achieved = nbytes / (ms / 1000.0) / 1e9
+    # CPU baseline: the oracle's gather_requant on a bounded sample of the same rows
+    import oracle
+
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from _helpers import oracle_cache, slots_of_tokens  # noqa: E402
+
+    tok = np.arange(8)
+    host_cache = oracle_cache(wl, rows=_kv_rows_for(wl, slots_of_tokens(wl, tok)))
+    v8 = wl.indices[tok] >= 0
+    hp = wl.indices[tok][v8].astype(np.int32)
+    hr = np.broadcast_to(wl.req_of_token[tok][:, None], v8.shape)[v8].astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.gather_requant(host_cache, wl.d_nope, wl.d_rope, hp, block_table=wl.block_table, page_size=wl.page_size,
+                          req_of_index=hr)
+    cpu_rows_s = hp.size / (time.perf_counter() - t0)
+    line = {
+        "metric": "gather-requant rows/s (256+0 FP8 paged)", "value": n / (ms / 1000.0), "unit": "rows/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": "requant_" + wl.name, "rows": n, "row_bytes": rb,
+                   "l2": "512 MB buffer written between timed steps (outside the events)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": None, "algorithmic_bytes_per_launch": nbytes},
+        "cpu_baseline": {"value": cpu_rows_s, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{hp.size} rows of 8 tokens"},
+        "gpu_launches": args.steps, "clocks": clk.summary(),
+        "step_ms": {"median": statistics.median(times), "min": min(times), "max": max(times)},
+    }
+    print(json.dumps(line))
+
+
 # ---------------------------------------------------------------------------- CPU oracle --
 class OracleRunner:
     """The CPU oracle (as it stands) on the workload. The packed cache rows the tokens name are
@@ -311,6 +387,8 @@ def main():
     ap.add_argument("--config", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--op", default="attn", choices=["attn", "requant"],
+                    help="requant: time dsa_gather_requant on the decode workload's rows instead")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -367,6 +445,12 @@ def main():
     __graft_entry__.build() if rank == 0 else None
     if world > 1:
         torch.distributed.barrier()
+    if args.op == "requant":
+        if rank == 0:
+            run_requant(args, device)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
     r = run_gpu(args, wl, rank, world, device)
     if rank != 0:
         if world > 1:

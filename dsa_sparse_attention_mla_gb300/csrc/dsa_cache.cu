@@ -180,10 +180,15 @@ __global__ void __launch_bounds__(256) gather_dequant_kernel(const uint8_t* __re
 }
 
 // ----------------------------------------------------------------- gather / requant kernel --
-// One warp per row: gather packed row indices[i] (direct or paged, as gather_dequant), widen each
-// tile to bf16_rne(fp32(e4m3(code)) * scale) exactly as gather_dequant does, and pack those
-// values again (pack_tile) into row out_loc[i] (or i) of `out`; RoPE bits are copied. A masked
-// index, or one that addresses no slot, packs the zero row.
+// One warp per kRqRows rows: gather packed row indices[i] (direct or paged, as gather_dequant),
+// widen each tile to bf16_rne(fp32(e4m3(code)) * scale) exactly as gather_dequant does, and pack
+// those values again (pack_tile) into row out_loc[i] (or i) of `out`; RoPE bits are copied. A
+// masked index, or one that addresses no slot, packs the zero row. The rows' index and page
+// lookups run on separate lanes at once, and the warp loads all its rows before converting any,
+// so that the dependent lookups and the row loads of many rows overlap.
+// rows per warp (16 for 264-byte rows measured slower: the registers cost occupancy)
+template <int D_NOPE>
+constexpr int rq_rows() { return 8; }
 template <int D_NOPE, int D_ROPE>
 __global__ void __launch_bounds__(256) gather_requant_kernel(const uint8_t* __restrict__ cache, int64_t num_slots,
                                                              const int32_t* __restrict__ indices, int64_t n,
@@ -194,40 +199,85 @@ __global__ void __launch_bounds__(256) gather_requant_kernel(const uint8_t* __re
                                                              int64_t out_slots, int32_t* error_word) {
   constexpr int TILES = D_NOPE / 128;
   constexpr int64_t RB = D_NOPE + 4 * TILES + 2 * D_ROPE;
+  constexpr int RW = D_ROPE / 2;  // RoPE words (<= 32: one per lane)
+  constexpr int kRqRows = rq_rows<D_NOPE>();
   const int lane = threadIdx.x & 31;
-  const int64_t i = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (i >= n) return;
-  const int64_t dslot = out_loc ? out_loc[i] : i;
-  if (dslot < 0 || dslot >= out_slots) {
-    if (lane == 0 && error_word) atomicOr(error_word, DSA_DEVERR_SLOT_OUT_OF_RANGE);
-    return;
-  }
-  const int64_t req = req_of_index ? req_of_index[i] : 0;
-  const int64_t slot = translate_slot(indices[i], req, num_slots, bt, bt_stride, page_size, max_pages);
-  if (slot == -2 && lane == 0 && error_word) atomicOr(error_word, DSA_DEVERR_INDEX_OUT_OF_RANGE);
-  const uint8_t* r = slot >= 0 ? cache + slot * RB : nullptr;
-  uint8_t* dst = out + dslot * RB;
-#pragma unroll
-  for (int j = 0; j < TILES; ++j) {
-    float x[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    if (r) {
-      const uint32_t c = *reinterpret_cast<const uint32_t*>(r + 128 * j + 4 * lane);
-      const float sc = *reinterpret_cast<const float*>(r + D_NOPE + 4 * j);
-      const float2 a = f16x2_to_f32x2(e4m3x2_to_f16x2((uint16_t)(c & 0xFFFFu)));
-      const float2 b = f16x2_to_f32x2(e4m3x2_to_f16x2((uint16_t)(c >> 16)));
-      const uint32_t w0 = f32x2_to_bf16x2(__fmul_rn(a.x, sc), __fmul_rn(a.y, sc));
-      const uint32_t w1 = f32x2_to_bf16x2(__fmul_rn(b.x, sc), __fmul_rn(b.y, sc));
-      x[0] = __uint_as_float(w0 << 16);
-      x[1] = __uint_as_float(w0 & 0xFFFF0000u);
-      x[2] = __uint_as_float(w1 << 16);
-      x[3] = __uint_as_float(w1 & 0xFFFF0000u);
+  const int64_t i0 = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * kRqRows;
+  if (i0 >= n) return;
+  // lane r < kRqRows resolves row i0 + r (destination, request, source slot) for the warp
+  int64_t my_d = -1, my_slot = -1;
+  if (lane < kRqRows && i0 + lane < n) {
+    const int64_t i = i0 + lane;
+    const int64_t d = out_loc ? out_loc[i] : i;
+    if (d < 0 || d >= out_slots) {
+      if (error_word) atomicOr(error_word, DSA_DEVERR_SLOT_OUT_OF_RANGE);
+    } else {
+      my_d = d;
+      const int64_t req = req_of_index ? req_of_index[i] : 0;
+      my_slot = translate_slot(indices[i], req, num_slots, bt, bt_stride, page_size, max_pages);
+      if (my_slot == -2 && error_word) atomicOr(error_word, DSA_DEVERR_INDEX_OUT_OF_RANGE);
     }
-    pack_tile(x, lane, dst + 128 * j, reinterpret_cast<float*>(dst + D_NOPE + 4 * j));
   }
-  if constexpr (D_ROPE > 0) {
-    uint32_t* rd = reinterpret_cast<uint32_t*>(dst + D_NOPE + 4 * TILES);
-    const uint32_t* rs = r ? reinterpret_cast<const uint32_t*>(r + D_NOPE + 4 * TILES) : nullptr;
-    for (int w = lane; w < D_ROPE / 2; w += 32) rd[w] = rs ? rs[w] : 0u;
+  uint32_t c[kRqRows][TILES];
+  float sc[kRqRows][TILES];
+  uint32_t rw[kRqRows];
+  int64_t dslot[kRqRows];
+#pragma unroll
+  for (int r = 0; r < kRqRows; ++r) {
+    dslot[r] = __shfl_sync(0xffffffffu, my_d, r);
+    const int64_t slot = __shfl_sync(0xffffffffu, my_slot, r);
+    rw[r] = 0u;
+#pragma unroll
+    for (int j = 0; j < TILES; ++j) {
+      c[r][j] = 0u;
+      sc[r][j] = 0.0f;
+    }
+    if (dslot[r] < 0 || slot < 0) continue;
+    const uint8_t* row = cache + slot * RB;
+#pragma unroll
+    for (int j = 0; j < TILES; ++j) {
+      c[r][j] = *reinterpret_cast<const uint32_t*>(row + 128 * j + 4 * lane);
+      sc[r][j] = *reinterpret_cast<const float*>(row + D_NOPE + 4 * j);
+    }
+    if (RW > 0 && lane < RW) rw[r] = reinterpret_cast<const uint32_t*>(row + D_NOPE + 4 * TILES)[lane];
+  }
+#pragma unroll
+  for (int r = 0; r < kRqRows; ++r) {
+    if (dslot[r] < 0) continue;  // (warp-uniform)
+    uint8_t* dst = out + dslot[r] * RB;
+#pragma unroll
+    for (int j = 0; j < TILES; ++j) {
+      // A tile as the pack writes it (a positive scale, largest code magnitude 448 = 0x7E) comes
+      // back with the same codes and the scale fp32(bf16_rne(448 * scale) / 448): its widened
+      // maximum is bf16_rne(448 * scale), and widening then dividing by the new scale moves every
+      // value by at most about 2^-7.9 relative, less than half the e4m3 spacing (2^-4.9 relative
+      // for normal codes, 2^-10 absolute for subnormal ones). Any other tile takes the general
+      // widen-and-pack path.
+      const uint32_t mag = c[r][j] & 0x7F7F7F7Fu;  // code magnitudes, one per byte
+      uint32_t cmax = max(max(mag & 0xFFu, (mag >> 8) & 0xFFu), max((mag >> 16) & 0xFFu, mag >> 24));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) cmax = max(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
+      const float s0 = sc[r][j];
+      // (the scale bounds keep 448 * scale and its bf16 rounding finite, and every non-zero
+      // product code * scale a normal number, where the error bound above holds)
+      if (cmax == 0x7Eu && s0 >= 0x1p-117f && s0 <= 7.0e35f) {
+        *reinterpret_cast<uint32_t*>(dst + 128 * j + 4 * lane) = c[r][j];
+        if (lane == 0) {
+          const uint32_t m = __float_as_uint(__fmul_rn(448.0f, s0));
+          const float amax = __uint_as_float(((m + 0x7FFFu + ((m >> 16) & 1u)) >> 16) << 16);  // bf16_rne
+          *reinterpret_cast<float*>(dst + D_NOPE + 4 * j) = __fdiv_rn(amax, 448.0f);
+        }
+        continue;
+      }
+      const float2 a = f16x2_to_f32x2(e4m3x2_to_f16x2((uint16_t)(c[r][j] & 0xFFFFu)));
+      const float2 b = f16x2_to_f32x2(e4m3x2_to_f16x2((uint16_t)(c[r][j] >> 16)));
+      const uint32_t w0 = f32x2_to_bf16x2(__fmul_rn(a.x, s0), __fmul_rn(a.y, s0));
+      const uint32_t w1 = f32x2_to_bf16x2(__fmul_rn(b.x, s0), __fmul_rn(b.y, s0));
+      const float x[4] = {__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xFFFF0000u), __uint_as_float(w1 << 16),
+                          __uint_as_float(w1 & 0xFFFF0000u)};
+      pack_tile(x, lane, dst + 128 * j, reinterpret_cast<float*>(dst + D_NOPE + 4 * j));
+    }
+    if (RW > 0 && lane < RW) reinterpret_cast<uint32_t*>(dst + D_NOPE + 4 * TILES)[lane] = rw[r];
   }
 }
 
@@ -340,7 +390,8 @@ dsa_status_t dsa_gather_requant(const void* cache, int64_t num_slots, int d_nope
   dsa_status_t st = current_device(&dev);
   if (st != DSA_OK) return st;
   const dim3 block(256);
-  const dim3 grid((unsigned)((n + 7) / 8));
+  const int64_t rows_per_block = 8 * (d_nope == 256 ? rq_rows<256>() : rq_rows<512>());
+  const dim3 grid((unsigned)((n + rows_per_block - 1) / rows_per_block));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const uint8_t* c = static_cast<const uint8_t*>(cache);
   uint8_t* o = static_cast<uint8_t*>(out);

@@ -148,8 +148,11 @@ def test_gather_requant_bit_exact(gpu, d_nope, d_rope):
     idx[:5] = [0, 1, 2, 3, 4]
     ref, bad = oracle.gather_requant(cache, d_nope, d_rope, idx)
     assert bad == 0
-    got = dsa.dsa_gather_requant(torch.from_numpy(cache).to(gpu), d_nope, d_rope, torch.from_numpy(idx).to(gpu))
-    assert np.array_equal(got.cpu().numpy(), ref)
+    got = dsa.dsa_gather_requant(torch.from_numpy(cache).to(gpu), d_nope, d_rope,
+                                 torch.from_numpy(idx).to(gpu)).cpu().numpy()
+    diff = np.argwhere(got != ref)
+    assert diff.size == 0, (len(diff), diff[:4].tolist(), got[tuple(diff[0])], ref[tuple(diff[0])],
+                            cache[idx[diff[0][0]], d_nope:d_nope + 4 * tiles].view(np.float32).tolist())
 
 
 def test_gather_requant_paged_scatter_and_errors(gpu):
@@ -184,3 +187,31 @@ def test_gather_requant_paged_scatter_and_errors(gpu):
                            out_loc=bad_loc, out=out, error_word=err)
     torch.cuda.synchronize()
     assert err.item() & dsa.DEVERR_SLOT_OUT_OF_RANGE
+
+
+@pytest.mark.parametrize("d_nope,d_rope", [(256, 0), (512, 64)])
+def test_gather_requant_non_canonical_rows_bit_exact(gpu, d_nope, d_rope):
+    """Rows the pack would never write (arbitrary codes without a 448 maximum, zero, negative,
+    huge and tiny scales) take the general widen-and-pack path: still the oracle's bytes."""
+    rng = np.random.default_rng(8)
+    n = 2000
+    rb = dsa.dsa_packed_row_bytes(d_nope, d_rope)
+    tiles = d_nope // 128
+    cache = rng.integers(0, 256, size=(n, rb), dtype=np.uint8)
+    codes = cache[:, :d_nope]
+    codes[(codes & 0x7F) == 0x7F] = 0x11                          # no NaN codes (out of contract)
+    codes[: n // 2] &= 0xBD                                       # half the rows: no 0x7E maximum
+    # scales across the whole range where 448 * scale stays finite in bf16 (wider ones give
+    # inf and NaN codes: outside the format), denormal ones included
+    sc = np.exp2(rng.uniform(-140, 118.5, size=(n, tiles))).astype(np.float32)
+    sc *= rng.choice(np.array([1, -1], dtype=np.float32), size=(n, tiles))
+    sc[::7, 0] = 0.0
+    cache[:, d_nope:d_nope + 4 * tiles] = sc.view(np.uint8).reshape(n, 4 * tiles)
+    idx = rng.permutation(n).astype(np.int32)
+    ref, bad = oracle.gather_requant(cache, d_nope, d_rope, idx)
+    assert bad == 0
+    got = dsa.dsa_gather_requant(torch.from_numpy(cache).to(gpu), d_nope, d_rope,
+                                 torch.from_numpy(idx).to(gpu)).cpu().numpy()
+    diff = np.argwhere(got != ref)
+    assert diff.size == 0, (len(diff), diff[:4].tolist(), got[tuple(diff[0])], ref[tuple(diff[0])],
+                            cache[idx[diff[0][0]], d_nope:d_nope + 4 * tiles].view(np.float32).tolist())
