@@ -326,7 +326,7 @@ def run_requant(args, device):
         "config": {"workload": "requant_" + wl.name, "rows": n, "row_bytes": rb,
                    "l2": "512 MB buffer written between timed steps (outside the events)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": None, "algorithmic_bytes_per_launch": nbytes},
+                     "traffic": _recorded_traffic("requant_" + wl.name), "algorithmic_bytes_per_launch": nbytes},
         "cpu_baseline": {"value": cpu_rows_s, "unit": "rows/s", "cores": 1, "kind": "oracle",
                          "sample": f"{hp.size} rows of 8 tokens"},
         "gpu_launches": args.steps, "clocks": clk.summary(),
