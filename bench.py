@@ -42,6 +42,26 @@ def _peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+def max_over_ranks(value: float, world: int) -> float:
+    """The largest of every rank's value (the job's time is its slowest rank's). The exchange
+    tensor lives where the process group's backend wants it: the GPU for NCCL, the host for gloo."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world: int, tokens_per_rank: int, steps: int, total_ms: float) -> float:
+    """Whole-job tokens/s: every rank processes its own copy of the workload (weak scaling), and
+    the job takes the slowest rank's time."""
+    return world * tokens_per_rank * steps / (total_ms / 1000.0)
+
+
 def _recorded_traffic(workload):
     """DRAM bytes per launch of the attention kernel for this workload, from the ncu capture
     recorded under profiles/, or None when there is none or the kernel sources have changed
@@ -225,11 +245,7 @@ def run_gpu(args, wl, rank, world, device):
     if world > 1:
         torch.distributed.barrier()
     times = [s.elapsed_time(e) for s, e in zip(starts, ends)]  # ms
-    total_ms = float(sum(times))
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(sum(times)), world)
     if err.item() != 0:
         raise RuntimeError(f"device error word {err.item()} during the benchmark")
 
@@ -458,7 +474,7 @@ def main():
         return
     hbm, bf16, bf16_sus, peak_src = _peaks()
     ms_per_step = r["total_ms"] / args.steps
-    value = world * wl.T * args.steps / (r["total_ms"] / 1000.0)
+    value = job_value(world, wl.T, args.steps, r["total_ms"])
     achieved = work["bytes"] / (ms_per_step / 1000.0) / 1e9
     tflops = work["flops"] / (ms_per_step / 1000.0) / 1e12
     cpu_v, cores, sample = OracleRunner(wl).sample(args.cpu_seconds)
