@@ -261,3 +261,14 @@ def test_balanced_split_causal_prefill(gpu):
     cache = oracle_cache(wl)
     again, _ = _gpu_attn(wl, cache, gpu)
     assert torch.equal(again.view(torch.int16), out.view(torch.int16))
+
+
+def test_balanced_split_with_every_entry_masked(gpu):
+    """Many tokens whose lists are all padding: the work-balanced split sees only the per-token
+    weights (no valid entry anywhere). Every output is zero and every lse -inf."""
+    T, topk = 2048, 2048
+    wl = W.bf16_direct(T=T, slots=512, topk=topk, n_valid=1, seed=90, sm_scale=1 / 16)
+    wl.indices[:] = -1
+    out, lse_t = _gpu_attn(wl, oracle_cache(wl), gpu, lse=True)
+    assert (f32_of(out) == 0).all()
+    assert np.isneginf(f32_of(lse_t)).all()

@@ -56,3 +56,26 @@ def test_static_scratch_argument_errors(dsa_lib):
     a.H, a.T = 64, 0
     assert dsa_lib.dsa_sparse_attn_static_ws(ctypes.byref(a), None) == 0   # nothing to do
     assert dsa_lib.dsa_sparse_attn_static_ws(None, None) == 1
+
+
+def test_static_scratch_with_the_work_balanced_split(gpu):
+    """Long causal lists (T=3072): the launch takes the work-balanced split, whose slice counts
+    and range bounds also live in the fixed scratch; two calls equal the workspace entry point
+    bit for bit (same bounds, same schedule)."""
+    wl = W.prefill_causal(T=3072, topk=2048, window=128, seed=31, name="prefill_causal_T3072")
+    cache = oracle_cache(wl)
+    q = bf16_dev(wl.q_bits(), gpu)
+    dcache = bf16_dev(cache, gpu)
+    idx = torch.from_numpy(wl.indices).to(gpu)
+    ref = dsa.dsa_sparse_attn(q, dcache, 0, idx, wl.sm_scale)
+    lib = dsa.load_library()
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for call in range(2):
+        out = torch.full_like(ref, float("nan"))
+        err = torch.zeros(1, dtype=torch.int32, device=gpu)
+        a = dsa._attn_args(q, dcache, 0, idx, wl.sm_scale, 256, 0, 256, None, 0, None, out, None, None, err)
+        st = lib.dsa_sparse_attn_static_ws(ctypes.byref(a), stream)
+        assert st == 0, dsa.dsa_status_string(st)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), f"call {call}"
