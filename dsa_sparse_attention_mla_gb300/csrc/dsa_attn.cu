@@ -216,7 +216,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       if (lane == 0) mbar_arrive(m_full(st));
       ++mc;
     };
-    constexpr int IPL = C::IDX_PER_LANE;
     const int64_t pos_limit = p.bt ? (int64_t)p.max_pages * p.page_size : p.num_slots;
     int64_t u = u0;
     while (u < u1 && !*abort_flag) {
@@ -940,7 +939,7 @@ static dsa_status_t get_encode_fn(EncodeTiledFn* fn) {
 }
 
 dsa_status_t encode_q_tensor_map(const dsa_attn_args_t* a, int dk, CUtensorMap* out) {
-  EncodeTiledFn encode;
+  EncodeTiledFn encode = nullptr;
   dsa_status_t st = get_encode_fn(&encode);
   if (st != DSA_OK) return st;
   const cuuint64_t dims[3] = {(cuuint64_t)dk, (cuuint64_t)kHeads, (cuuint64_t)a->T};
