@@ -28,10 +28,12 @@
 //    contiguous ranges per CTA; a token cut by a range boundary is merged in-kernel by the CTA
 //    holding its first tiles (fixed order, no atomics on data).
 //  * Warp roles: 0 producer (index read, -1 compaction into dense 128-key tiles, page
-//    translation, Q loads by TMA), 1 score-MMA issuer, 2 output-MMA issuer, 4-7 softmax and
-//    epilogue, 3 and 8-15 row loaders (cp.async copies of bf16 rows straight into the tile, or
-//    of packed half rows into a ring, widened into the 128-byte-swizzled K tile). Packed rows
-//    are not prefetched into L2: the extra whole-line traffic cost more than it saved.
+//    translation, Q loads by TMA), 1 score-MMA issuer, 2 output-MMA issuer, then softmax and
+//    epilogue warps and row loaders: for packed rows 4-7 softmax, 3 and 8-15 loaders (copies of
+//    packed half rows into a ring, widened into the 128-byte-swizzled K tile); for bf16 rows,
+//    whose loaders only issue cp.async copies straight into the tile, 4-11 softmax (two warps
+//    per TMEM lane quarter, 32 heads each) and 3, 12-15 loaders. Packed rows are not prefetched
+//    into L2: the extra whole-line traffic cost more than it saved.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -51,14 +53,8 @@ constexpr int kD = 256;         // latent width (= d_v)
 constexpr int kBN = 128;        // gathered keys per tile: MMA M
 constexpr int kKST = 2;         // K tile stages
 constexpr int kMST = 8;         // meta ring depth
-constexpr int kNSM = 4;         // softmax warps (4-7): one per TMEM lane quarter
-constexpr int kHW = kH * 4 / kNSM;  // heads per softmax warp
-constexpr int kCH = kHW / 16;       // 16-head chunks per softmax warp
-constexpr int kNLD = 9;         // loader warps: 3 and 8-15
 constexpr int kWarps = 16;
 constexpr int kThreads = 32 * kWarps;
-// loader warp index (3 -> 0, 8..15 -> 1..8), -1 for other warps
-__device__ __forceinline__ int loader_index(int warp) { return warp == 3 ? 0 : (warp >= 8 ? warp - 7 : -1); }
 constexpr int kMaxParts = 16;     // most parts of one split token (the launch guarantees it)
 constexpr int kRing = 8;          // ring of a packed-row loader warp: 2 units of 8 half rows (2 KB)
 constexpr uint64_t kWaitNs = 2000000000ull;
@@ -73,6 +69,19 @@ template <int KIND>
 struct Cfg {
   static constexpr bool FP8 = KIND == DSA_CACHE_FP8_SCALED;
   static constexpr int RB = FP8 ? 264 : 512;  // cache row bytes
+  // Warp roles: 0 producer, 1 score-MMA issuer, 2 output-MMA issuer, 4 .. 3 + NSM softmax (warp
+  // w takes TMEM lane quarter w % 4; with eight, the two warps of a quarter split the heads), 3
+  // and 4 + NSM .. 15 row loaders. Packed rows need nine loader warps for their dequantisation;
+  // bf16 rows are plain copies, and their warps go to the softmax instead.
+  static constexpr int NSM = FP8 ? 4 : 8;
+  static constexpr int NLD = kWarps - 3 - NSM;
+  static constexpr int HW = kH * 4 / NSM;  // heads per softmax warp
+  static constexpr int CH = HW / 16;       // 16-head chunks per softmax warp
+  static constexpr int NR = (kBN + NLD - 1) / NLD;  // most rows of a tile per loader warp
+  // loader index of a warp (3 -> 0, 4 + NSM .. 15 -> 1 ..), -1 for other warps
+  static __device__ __forceinline__ int loader_index(int warp) {
+    return warp == 3 ? 0 : (warp >= 4 + NSM ? warp - 3 - NSM : -1);
+  }
   static constexpr int NSUB = FP8 ? 2 : 1;    // score accumulators per tile (one per scale tile)
   static constexpr int PBUF = FP8 ? 1 : 2;    // P buffers
   static constexpr int P_BYTES = NSUB * kBN * 128;
@@ -88,10 +97,10 @@ struct Cfg {
   static constexpr int META_BYTES = 32 + 4 * kBN;
   static constexpr int CMP_OFF = META_OFF + kMST * META_BYTES;  // producer: one step's valid slots
   static constexpr int RING_OFF = CMP_OFF + 4 * 256;                // packed-row loaders: code rings
-  static constexpr int RING_BYTES = FP8 ? kNLD * kRing * 256 : 0;
+  static constexpr int RING_BYTES = FP8 ? NLD * kRing * 256 : 0;
   static constexpr int RED_OFF = RING_OFF + RING_BYTES;
   // m[64], alpha[64], lsum[64], spare[64], part[4][64], wk[kMaxParts][64], votes[2][8]
-  static constexpr int RED_FLOATS = 8 * kH + kMaxParts * kH + 2 * kNSM;
+  static constexpr int RED_FLOATS = 8 * kH + kMaxParts * kH + 2 * NSM;
   static constexpr int SPLIT_OFF = RED_OFF + ((RED_FLOATS * 4 + 15) & ~15);  // producer: range bounds
   static constexpr int BAR_OFF = SPLIT_OFF + 8 * (kSplitMaxCtas + 1);
   static constexpr int NBARS = 2 + 4 * kKST + 2 * kMST + 8 + 3;
@@ -164,18 +173,19 @@ __device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
 // Exchange among the softmax warps (one arrival each on `xbar`, phase `n` of it; `sm` is the
 // warp's softmax index): returns the OR of `v` over the warps, with every warp's earlier
 // shared-memory writes visible, or -1 when a warp did not arrive within the time limit.
+template <int NSM>
 static __device__ __noinline__ int softmax_exchange(uint32_t xbar, int* votes, uint32_t n, int sm, int v) {
   const int lane = threadIdx.x & 31;
   const int slot = n & 1;
   const bool any = __any_sync(0xffffffffu, v != 0);
-  if (lane == 0) votes[slot * kNSM + sm] = any ? 1 : 0;
+  if (lane == 0) votes[slot * NSM + sm] = any ? 1 : 0;
   __syncwarp();
   if (lane == 0) mbar_arrive(xbar);
   const bool ok = mbar_wait(xbar, n & 1, kWaitNs);
   if (!__all_sync(0xffffffffu, ok)) return -1;
   int r = 0;
 #pragma unroll
-  for (int w = 0; w < kNSM; ++w) r |= votes[slot * kNSM + w];
+  for (int w = 0; w < NSM; ++w) r |= votes[slot * NSM + w];
   return r ? 1 : 0;
 }
 
@@ -211,21 +221,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kKST; ++s) {
       for (int h = 0; h < 2; ++h) {
         // bf16 rows: one cp.async arrive per loader thread; packed rows: one per loader warp
-        mbar_init(k_full(s, h), C::FP8 ? kNLD : 32 * kNLD);
+        mbar_init(k_full(s, h), C::FP8 ? C::NLD : 32 * C::NLD);
         mbar_init(k_empty(s, h), 1);
       }
     }
     for (int s = 0; s < kMST; ++s) {
       mbar_init(m_full(s), 1);
-      mbar_init(m_empty(s), 2 + kNSM + kNLD);  // 2 MMA threads, softmax warps, loader warps
+      mbar_init(m_empty(s), 2 + C::NSM + C::NLD);  // 2 MMA threads, softmax warps, loader warps
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(s_full(i), 1);
-      mbar_init(s_empty(i), kNSM);
-      mbar_init(p_full(i), kNSM);
+      mbar_init(s_empty(i), C::NSM);
+      mbar_init(p_full(i), C::NSM);
       mbar_init(pv_done(i), 1);
     }
-    mbar_init(xbar, kNSM);
+    mbar_init(xbar, C::NSM);
     mbar_init(mma_drain, 1);
     mbar_init(mma_drain + 8, 1);
     *abort_flag = 0;
@@ -557,18 +567,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(drain, 0, kWaitNs);
     }
     __syncwarp();
-  } else if (warp >= 4 && warp < 4 + kNSM) {  // (softmax)
-    // ============================================== softmax + epilogue (8 warps) ====
-    // Thread = key of the tile = TMEM lane (quarter warp % 4); the two warps of a quarter take
-    // heads 0-31 and 32-63. Per tile one pass computes, with the running max m_h of each head,
+  } else if (warp >= 4 && warp < 4 + C::NSM) {  // (softmax)
+    // ================================== softmax + epilogue (4 or 8 warps, C::NSM) ====
+    // Thread = key of the tile = TMEM lane (quarter warp % 4); with eight warps the two warps
+    // of a quarter take heads 0-31 and 32-63. Per tile one pass computes, with the running max m_h of each head,
     // x = c * score - m_h, p = 2^x, the per-lane partial row sums (TMEM, two buffers: the pass
-    // reads one and writes the other) and the probability rows of P. A vote of the eight warps
+    // reads one and writes the other) and the probability rows of P. A vote of the warps
     // then checks that no x exceeded 8; if one did (rare after a segment's first tile), the
     // tile takes exact per-head maxima, raises m_h where it grew by more than 2^8, rescales O
     // and the partial sums of those heads, and is redone. A segment's first tile starts there.
     const int sm = warp - 4;                                 // softmax warp index
     const int qd = warp & 3;                                 // TMEM lane quarter
-    const int hb = kHW * (sm >> 2);                          // first head of this warp
+    const int hb = C::HW * (sm >> 2);                          // first head of this warp
     const int tr = 32 * qd + lane;                           // key row of the tile / dv row of O^T
     const int sid = 32 * sm + lane;                          // softmax thread index
     const uint32_t tl = tmem + ((uint32_t)(32 * qd) << 16);  // this warp's lanes
@@ -577,10 +587,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* red_alpha = red + 64;  // rescale factor per head; epilogue: weight of own partial
     float* red_part = red + 256;  // [4 lane quarters][64 heads]
     float* red_wk = red + 512;    // [kMaxParts][64]: merge weights of the other parts
-    int* votes = reinterpret_cast<int*>(red + 512 + kMaxParts * kH);  // [2][kNSM]
+    int* votes = reinterpret_cast<int*>(red + 512 + kMaxParts * kH);  // [2][C::NSM]
     uint32_t mc = 0, g = 0, xc = 0, lb = 0;
     auto xsync = [&](bool v) -> int {
-      const int r = softmax_exchange(xbar, votes, xc++, sm, v ? 1 : 0);
+      const int r = softmax_exchange<C::NSM>(xbar, votes, xc++, sm, v ? 1 : 0);
       if (r < 0) fail(DSA_DEVERR_TIMEOUT);
       return r;
     };
@@ -642,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // exact per-head maximum of this tile: warp max-reductions over the keys, then
             // across the four lane quarters
 #pragma unroll 1
-            for (int ch = 0; ch < kCH; ++ch) {
+            for (int ch = 0; ch < C::CH; ++ch) {
               uint32_t a[16], bb[16];
               tmem_ld32_x16(sa + 16 * ch, a);
               if constexpr (C::FP8) tmem_ld32_x16(sa + 64 + 16 * ch, bb);
@@ -673,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!wait_all(pv_wait((int64_t)g - 1))) { bad = true; break; }
             tc_fence_after();
 #pragma unroll 1
-            for (int ch = 0; ch < kCH; ++ch) {
+            for (int ch = 0; ch < C::CH; ++ch) {
               uint32_t o0[16], o1[16], lv[16];
               tmem_ld32_x16(tl + C::O_COL + hb + 16 * ch, o0);
               tmem_ld32_x16(tl + C::O_COL + 64 + hb + 16 * ch, o1);
@@ -697,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // and P (packed rows: p * scale of each tile) as bf16 into this key's 128-byte row
           float xm = -INFINITY;
 #pragma unroll 1
-          for (int ch = 0; ch < kCH; ++ch) {
+          for (int ch = 0; ch < C::CH; ++ch) {
             float mv[16];  // running maxima of the chunk's heads, read ahead of the TMEM wait
 #pragma unroll
             for (int i = 0; i < 16; i += 4)
@@ -767,7 +777,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // over the other); lane 2i writes it to red_part[quarter][head], and thread h < 64 adds
       // up the quarters
 #pragma unroll 1
-      for (int ch = 0; ch < kCH; ++ch) {
+      for (int ch = 0; ch < C::CH; ++ch) {
         uint32_t l[16];
         if (had) {
           tmem_ld32_x16(lfin + 16 * ch, l);
@@ -808,7 +818,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float* w0 = p.ws_o + ((int64_t)b * kD + tr) * kH + hb;
           float* w1 = p.ws_o + ((int64_t)b * kD + 128 + tr) * kH + hb;
 #pragma unroll 1
-          for (int ch = 0; ch < kCH; ++ch) {
+          for (int ch = 0; ch < C::CH; ++ch) {
             uint32_t o0[16], o1[16];
             tmem_ld32_x16(tl + C::O_COL + hb + 16 * ch, o0);
             tmem_ld32_x16(tl + C::O_COL + 64 + hb + 16 * ch, o1);
@@ -832,10 +842,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool okp = true;
       // every publish flag of parts b+1 .. last, one per lane (a warp vote ends the wait); the
       // warp barrier then orders every lane's reads of the parts after the acquiring loads
-      for (int f0 = 0; f0 < nparts * kNSM && okp; f0 += 32) {
+      for (int f0 = 0; f0 < nparts * C::NSM && okp; f0 += 32) {
         const int f = f0 + lane;
-        const bool mine = f < nparts * kNSM;
-        const int* fp = p.flags + 8 * (b + 1 + f / kNSM) + f % kNSM;
+        const bool mine = f < nparts * C::NSM;
+        const int* fp = p.flags + 8 * (b + 1 + f / C::NSM) + f % C::NSM;
         const uint64_t t0 = globaltimer_ns();
         for (;;) {
           int v = p.epoch;
@@ -873,7 +883,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // combine and stage the bf16 block [64 heads][256 columns] in the (idle) P buffers
       uint16_t* stage = reinterpret_cast<uint16_t*>(smem + C::P_OFF);
 #pragma unroll 1
-      for (int ch = 0; ch < kCH; ++ch) {
+      for (int ch = 0; ch < C::CH; ++ch) {
         const int h0 = hb + 16 * ch;
         float acc0[16], acc1[16];
         const float* wo = red_alpha + h0;
@@ -920,17 +930,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         uint16_t* orow = p.out + t * p.out_st;
 #pragma unroll 4
-        for (int j = 0; j < 2048 / (32 * kNSM); ++j) {
-          const int q = sid + 32 * kNSM * j, h = q >> 5, gq = q & 31;
+        for (int j = 0; j < 2048 / (32 * C::NSM); ++j) {
+          const int q = sid + 32 * C::NSM * j, h = q >> 5, gq = q & 31;
           *reinterpret_cast<uint4*>(orow + (int64_t)h * p.out_sh + gq * 8) =
               *reinterpret_cast<const uint4*>(stage + h * kD + gq * 8);
         }
       }
       tc_fence_before();
     }
-  } else if (loader_index(warp) >= 0) {
-    // ====================================================== row loaders (9 warps) ====
-    // Warp dw fills rows dw + kNLD * k (k < nk) of each K tile in the 128-byte-swizzled K-major
+  } else if (C::loader_index(warp) >= 0) {
+    // ================================================= row loaders (C::NLD warps) ====
+    // Warp dw fills rows dw + C::NLD * k (k < nk) of each K tile in the 128-byte-swizzled K-major
     // layout (row r, 16-byte granule q of 64-column chunk c at c*128*128 + r*128 + ((q ^ (r&7)) << 4)).
     // A tile is written in two column halves, columns 0-127 (chunks 0-1) and 128-255 (chunks
     // 2-3), each with its own full and empty barrier: the score product starts on the first half
@@ -939,9 +949,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 16-31: row 2p + 1); lane il of a half warp handles 16-byte granule 16h + il of its row, so
     // the eight lanes of a quarter warp store to eight different 16-byte positions.
     // Rows past n_valid are zero (their keys are masked: a zero row keeps 0 * V finite).
-    const int dw = loader_index(warp);
-    const int nk = (kBN - dw + kNLD - 1) / kNLD;  // rows of this warp per tile: dw + kNLD * k, k < nk
-    static_assert((kBN + kNLD - 1) / kNLD <= 16, "a warp's rows of a tile fit eight row pairs");
+    const int dw = C::loader_index(warp);
+    const int nk = (kBN - dw + C::NLD - 1) / C::NLD;  // rows of this warp per tile: dw + C::NLD * k, k < nk
+    // lane t holds the slot of row dw + NLD * t; packed rows are taken as eight row pairs
+    static_assert(C::NR <= (C::FP8 ? 16 : 32), "a warp's rows of a tile fit its lanes");
     const int hl = lane >> 4, il = lane & 15;
     uint32_t mc = 0, g = 0;
     auto next_tile = [&](bool block, int& st_out) -> int {
@@ -962,7 +973,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return 0;
     };
-    // tile in meta slot st: row count, lane t's slot of row dw + kNLD * t (-1 past the valid
+    // tile in meta slot st: row count, lane t's slot of row dw + C::NLD * t (-1 past the valid
     // rows) and, for packed rows, its two scales. Everything the loader needs of the entry is
     // then in registers: the caller releases the meta stage right away, and a copy takes the
     // slot of row k from lane k by a shuffle.
@@ -970,7 +981,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const MetaHdr* mh = reinterpret_cast<const MetaHdr*>(smem + C::META_OFF + st * C::META_BYTES);
       n = mh->n_valid;
       const int* slots = reinterpret_cast<const int*>(reinterpret_cast<const uint8_t*>(mh) + 32);
-      const int rt = dw + kNLD * lane;
+      const int rt = dw + C::NLD * lane;
       slr = -1;
       scale = make_float2(0.0f, 0.0f);
       if (lane < nk && rt < n) {
@@ -1001,11 +1012,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const int G = 16 * h + il;
 #pragma unroll
-          for (int pp = 0; pp < 8; ++pp) {
+          for (int pp = 0; pp < (C::NR + 1) / 2; ++pp) {
             const int k = 2 * pp + hl;
             const int sl = __shfl_sync(0xffffffffu, slr, k);
             if (k < nk) {
-              const int r = dw + kNLD * k;
+              const int r = dw + C::NLD * k;
               const uint8_t* src = p.cache + (sl >= 0 ? (int64_t)sl : 0) * (2 * kD) + 16 * G;
               const uint32_t dst = smem_u32(kt + (G >> 3) * (kBN * 128) + r * 128 + (((G & 7) ^ (r & 7)) << 4));
               asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(sl >= 0 ? 16 : 0)
@@ -1081,7 +1092,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int G = 16 * h + il;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const int k = 2 * (4 * (u & 1) + q) + hl, rr = dw + kNLD * k;
+            const int k = 2 * (4 * (u & 1) + q) + hl, rr = dw + C::NLD * k;
             uint4 o = make_uint4(e4m3x2_to_bf16x2_exact<0x9180u>(w[q].x), e4m3x2_to_bf16x2_exact<0xB3A2u>(w[q].x),
                                  e4m3x2_to_bf16x2_exact<0x9180u>(w[q].y), e4m3x2_to_bf16x2_exact<0xB3A2u>(w[q].y));
             if (!full && rr >= n_c) o = make_uint4(0u, 0u, 0u, 0u);
@@ -1096,7 +1107,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (u & 1) {  // column half h of the tile is written
             if (h == 1 && lane < nk)
-              *reinterpret_cast<float2*>(smem + C::SC_OFF + ks * C::SC_BYTES + (dw + kNLD * lane) * 8) = sc_c;
+              *reinterpret_cast<float2*>(smem + C::SC_OFF + ks * C::SC_BYTES + (dw + C::NLD * lane) * 8) = sc_c;
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(k_full(ks, h));

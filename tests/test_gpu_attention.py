@@ -229,13 +229,14 @@ def _scaled_halves(bits, lo, hi):
     return (f.view(np.uint32) >> 16).astype(np.uint16)
 
 
-@pytest.mark.parametrize("e", [10, -10])
+@pytest.mark.parametrize("e", [10, -10, 16, -16])
 def test_fp8_tile_scales_applied_per_tile(gpu, e):
-    """Rows whose two 128-column tiles differ in magnitude by 2^20, so that their tile scales do,
-    with the query scaled inversely (scores stay of order one): the kernel applies each tile's
-    fp32 scale to its own half of the score and of the output. Each output half is compared
-    after undoing its exact power-of-two factor, i.e. at the precision of the unscaled problem;
-    the LSE is unaffected by the value scaling and is checked as is."""
+    """Rows whose two 128-column tiles differ in magnitude by 2^(2e), so that their tile scales
+    do, with the query scaled inversely (scores stay of order one): the kernel applies each
+    tile's fp32 scale to its own half of the score and of the output (at |e| = 16 one tile's
+    scales are about 2^9, the other's about 2^-23). Each output half is compared after undoing
+    its exact power-of-two factor, i.e. at the precision of the unscaled problem; the LSE is
+    unaffected by the value scaling and is checked as is."""
     wl = W.fp8_paged(T=6, requests=1, positions=4096, page_size=64, topk=2112, n_valid=2051, seed=15, sm_scale=1 / 16)
     wl.kv = W.FixedRows(_scaled_halves(wl.kv.bits(), -e, e))
     wl.q = W.FixedRows(_scaled_halves(wl.q.bits(), e, -e))
@@ -245,6 +246,33 @@ def test_fp8_tile_scales_applied_per_tile(gpu, e):
     assert bad == 0
     undo = np.concatenate([np.full(128, 2.0 ** e), np.full(128, 2.0 ** -e)])
     check_close(f32_of(out) * undo, ref * undo, "fp8 tile scales")
+    _check_lse(f32_of(lse_t), ref_lse, 2e-4)
+
+
+def test_fp8_large_scale_rows_among_ordinary_ones(gpu):
+    """Every seventh row has its second tile replaced by its magnitude times 2^15 (tile scales
+    above 2^7), the query's second half scaled by 2^-15: one loader warp holds rows with scales
+    2^15 apart in the same tile half, and each row's scale must reach only that row. Those rows
+    dominate the second half of the output; their values there are positive, so the output is
+    a sum without cancellation and keeps the precision of its terms (signed values of that size
+    would cancel to outputs far smaller than the terms, below what bf16 probabilities resolve).
+    Output and LSE against the exact oracle."""
+    wl = W.fp8_paged(T=5, requests=1, positions=4096, page_size=64, topk=2048, n_valid=2048, seed=16, sm_scale=1 / 16)
+    kv = (wl.kv.bits().astype(np.uint32) << 16).view(np.float32).copy()
+    kv[::7, 128:] = np.abs(kv[::7, 128:]) * 2.0 ** 15
+    wl.kv = W.FixedRows((kv.view(np.uint32) >> 16).astype(np.uint16))
+    q = (wl.q.bits().astype(np.uint32) << 16).view(np.float32).copy()
+    q[:, 128:] *= 2.0 ** -15
+    wl.q = W.FixedRows((q.view(np.uint32) >> 16).astype(np.uint16))
+    cache = oracle_cache(wl)
+    scales = cache[:, 256:264].copy().view(np.float32)
+    big = np.zeros(wl.num_slots, dtype=bool)
+    big[::7] = True
+    assert scales[wl.kv_slot[big], 1].min() >= 128.0 and scales[wl.kv_slot[~big], 1].max() < 128.0
+    out, lse_t = _gpu_attn(wl, cache, gpu, lse=True)
+    ref, ref_lse, bad = run_oracle(wl, cache)
+    assert bad == 0
+    check_close(f32_of(out), ref, "fp8 large-scale rows")
     _check_lse(f32_of(lse_t), ref_lse, 2e-4)
 
 
