@@ -43,3 +43,18 @@ def test_kernels_per_call_follows_the_launch_rule():
     assert bench.kernels_per_call(W.config(3), 152) == 1
     assert bench.kernels_per_call(W.config(4), 152) == 3
     assert bench.kernels_per_call(W.config(5), 152) == 1
+
+
+def test_roofline_bound_follows_the_stricter_term():
+    # decode gathers distinct rows of a 2.2 GB table: memory-bound, and every gathered byte is
+    # unique; causal prefill re-gathers a 4 MB table: the tensor term is the slower one
+    w3 = bench.algorithmic_work(W.config(3))
+    assert w3["unique_bytes"] == w3["bytes"]
+    r3 = bench.roofline(w3, 100e-6, 6759.9, 1905.3)
+    assert r3["bound"] == "hbm" and r3["unit"] == "GB/s"
+    assert abs(r3["achieved"] - w3["bytes"] / 100e-6 / 1e9) < 1e-6 * r3["achieved"]
+    w4 = bench.algorithmic_work(W.config(4))
+    assert w4["unique_bytes"] == 8192 * 512 + 8192 * 64 * 256 * 2 * 2 + W.config(4).indices.size * 4
+    r4 = bench.roofline(w4, 1.6e-3, 6759.9, 1905.3)
+    assert r4["bound"] == "tensor" and r4["unit"] == "TFLOP/s"
+    assert abs(r4["frac"] - w4["flops"] / 1.6e-3 / 1e12 / 1905.3) < 1e-12
