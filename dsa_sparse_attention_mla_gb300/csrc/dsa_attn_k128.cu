@@ -29,7 +29,7 @@
 //    holding its first tiles (fixed order, no atomics on data).
 //  * Warp roles: 0 producer (index read, -1 compaction into dense 128-key tiles, page
 //    translation, Q loads by TMA), 1 score-MMA issuer, 2 output-MMA issuer, then softmax and
-//    epilogue warps and row loaders: for packed rows 4-7 softmax, 3 and 8-15 loaders (copies of
+//    epilogue warps and row loaders: for packed rows 4-7 softmax, 8-15 loaders (copies of
 //    packed half rows into a ring, widened into the 128-byte-swizzled K tile); for bf16 rows,
 //    whose loaders only issue cp.async copies straight into the tile, 4-11 softmax (two warps
 //    per TMEM lane quarter, 32 heads each) and 3, 12-15 loaders. Packed rows are not prefetched
@@ -70,17 +70,21 @@ struct Cfg {
   static constexpr bool FP8 = KIND == DSA_CACHE_FP8_SCALED;
   static constexpr int RB = FP8 ? 264 : 512;  // cache row bytes
   // Warp roles: 0 producer, 1 score-MMA issuer, 2 output-MMA issuer, 4 .. 3 + NSM softmax (warp
-  // w takes TMEM lane quarter w % 4; with eight, the two warps of a quarter split the heads), 3
-  // and 4 + NSM .. 15 row loaders. Packed rows need nine loader warps for their dequantisation;
-  // bf16 rows are plain copies, and their warps go to the softmax instead.
+  // w takes TMEM lane quarter w % 4; with eight, the two warps of a quarter split the heads),
+  // then the row loaders. Packed rows: four softmax warps and eight loaders, warps 8-15, two on
+  // each SM sub-partition (warp w runs on sub-partition w % 4), which their dequantisation
+  // needs; warp 3 stays idle, since a ninth loader beside softmax warp 7 slows the warp that
+  // every tile's vote waits for. bf16 rows are plain copies: eight softmax warps and five
+  // loaders, warps 3 and 12-15.
   static constexpr int NSM = FP8 ? 4 : 8;
-  static constexpr int NLD = kWarps - 3 - NSM;
+  static constexpr int NLD = FP8 ? 8 : 5;
   static constexpr int HW = kH * 4 / NSM;  // heads per softmax warp
   static constexpr int CH = HW / 16;       // 16-head chunks per softmax warp
   static constexpr int NR = (kBN + NLD - 1) / NLD;  // most rows of a tile per loader warp
-  // loader index of a warp (3 -> 0, 4 + NSM .. 15 -> 1 ..), -1 for other warps
+  // loader index of a warp, -1 for other warps
   static __device__ __forceinline__ int loader_index(int warp) {
-    return warp == 3 ? 0 : (warp >= 4 + NSM ? warp - 3 - NSM : -1);
+    if constexpr (FP8) return warp >= 8 ? warp - 8 : -1;
+    else return warp == 3 ? 0 : (warp >= 12 ? warp - 11 : -1);
   }
   static constexpr int NSUB = FP8 ? 2 : 1;    // score accumulators per tile (one per scale tile)
   static constexpr int PBUF = FP8 ? 1 : 2;    // P buffers
