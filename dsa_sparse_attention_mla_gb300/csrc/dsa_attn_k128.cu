@@ -770,10 +770,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(m_empty(st));
       ++mc;
-      if (had) {
-        if (!wait_all(pv_wait((int64_t)g - 1))) break;
-        tc_fence_after();
-      }
+      // the row sums need only the partial-sum buffer the last pass wrote (this warp's own
+      // TMEM stores, complete before it signalled P): they run while the last output product
+      // may still be in flight, and O is read only after it
       const uint32_t lfin = tl + C::L_COL + 64 * lb + hb;  // the buffer the last pass wrote
       // row sums: per warp, a reduce-scatter over the lanes (keys) of each 16-head chunk leaves
       // the warp's sum of head 16 ch + (lane >> 1) in lanes 2i and 2i + 1 (each round halves the
@@ -811,7 +810,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         lsum = (red_part[sid] + red_part[64 + sid]) + (red_part[128 + sid] + red_part[192 + sid]);
         mrow = red_m[sid];
       }
-      if (xsync(false) < 0) break;  // the quarter sums are read before a next tile reuses them
+      // the quarter sums are read before a next tile's exact path rewrites them: a part publishes
+      // and moves on, so it needs its own exchange here; the other kinds pass the weights'
+      // exchange below after their last read
+      if (kind == kPart && xsync(false) < 0) break;
+      if (had) {
+        if (!wait_all(pv_wait((int64_t)g - 1))) break;
+        tc_fence_after();
+      }
       if (kind == kPart) {
         // publish (O^T, m, l) of this part in workspace slot b
         if (sid < kH) {
