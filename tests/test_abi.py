@@ -5,7 +5,6 @@ import os
 import re
 import subprocess
 
-import pytest
 
 import dsa_sparse_attention_mla_gb300 as dsa
 

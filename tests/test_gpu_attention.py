@@ -8,7 +8,6 @@ import numpy as np
 import pytest
 import torch
 
-import oracle
 import dsa_sparse_attention_mla_gb300 as dsa
 from dsa_sparse_attention_mla_gb300 import workloads as W
 

@@ -3,7 +3,6 @@ tokens name, packed by the oracle from the seeded source rows, indices remapped 
 page table) gives the same result as the oracle over the whole cache."""
 import numpy as np
 
-import oracle
 from dsa_sparse_attention_mla_gb300 import workloads as W
 
 from _helpers import oracle_cache, run_oracle

@@ -10,7 +10,6 @@ first left them in a usable state. This file is collected last on purpose.
 """
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
