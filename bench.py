@@ -31,6 +31,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 L2_FLUSH_BYTES = 512 << 20
+NOMINAL_HBM_GBS = 7900.0
+NOMINAL_BF16_TFLOPS = 2250.0
+METRIC = "sparse-attn tokens/s (256+0 FP8, T=256)"
 
 
 def _peaks():
@@ -234,7 +237,7 @@ def build_device_inputs(wl, device):
     return q, cache, idx, bt, req
 
 
-def run_gpu(args, wl, rank, world, device):
+def run_gpu(args, wl, rank, world, device, config):
     import torch
 
     import dsa_sparse_attention_mla_gb300 as dsa
@@ -307,7 +310,7 @@ def run_gpu(args, wl, rank, world, device):
     # steps' gathered rows (four times a step's) cannot be served from L2 without a flush.
     from dsa_sparse_attention_mla_gb300 import workloads as W
 
-    idx_sets = [idx_h] + [torch.from_numpy(W.config(args.config, seed=sd).indices).pin_memory() for sd in (1, 2, 3)]
+    idx_sets = [idx_h] + [torch.from_numpy(W.config(config, seed=sd).indices).pin_memory() for sd in (1, 2, 3)]
     s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
     qd = [torch.empty_like(q) for _ in range(2)]
     idd = [torch.empty_like(idx) for _ in range(2)]
@@ -395,12 +398,10 @@ def run_requant(args, device):
     achieved = nbytes / (ms / 1000.0) / 1e9
     # CPU baseline: the oracle's gather_requant on a bounded sample of the same rows
     import oracle
-
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from _helpers import oracle_cache, slots_of_tokens  # noqa: E402
+    from oracle.workload_inputs import cache_for_tokens
 
     tok = np.arange(8)
-    host_cache = oracle_cache(wl, rows=_kv_rows_for(wl, slots_of_tokens(wl, tok)))
+    host_cache = cache_for_tokens(wl, tok)
     v8 = wl.indices[tok] >= 0
     hp = wl.indices[tok][v8].astype(np.int32)
     hr = np.broadcast_to(wl.req_of_token[tok][:, None], v8.shape)[v8].astype(np.int32)
@@ -417,7 +418,7 @@ def run_requant(args, device):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "traffic": _recorded_traffic("requant_" + wl.name), "algorithmic_bytes_per_launch": nbytes},
         "cpu_baseline": {"value": cpu_rows_s, "unit": "rows/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{hp.size} rows of 8 tokens"},
+                         "sample": f"{hp.size} rows of 8 tokens", "cpu": cpu_model()},
         "gpu_launches": args.steps, "clocks": clk.summary(),
         "step_ms": {"median": statistics.median(times), "min": min(times), "max": max(times)},
     }
@@ -429,16 +430,14 @@ class OracleRunner:
     """The CPU oracle (as it stands) on the workload. The packed cache rows the tokens name are
     generated and packed by the oracle on the host: no oracle input comes from the GPU path."""
 
-    def __init__(self, wl):
+    def __init__(self, wl, tokens=None):
         import oracle
-
-        sys.path.insert(0, os.path.join(ROOT, "tests"))
-        from _helpers import oracle_cache, slots_of_tokens  # noqa: E402
+        from oracle.workload_inputs import cache_for_tokens
 
         self.oracle = oracle
         self.wl = wl
         self.q = wl.q_bits()
-        self.cache = oracle_cache(wl, rows=_kv_rows_for(wl, slots_of_tokens(wl, np.arange(wl.T))))
+        self.cache = cache_for_tokens(wl, np.arange(wl.T) if tokens is None else np.asarray(tokens))
         self.order = np.random.default_rng(1234).permutation(wl.T)
         self.threads = oracle.max_threads()
 
@@ -459,13 +458,74 @@ class OracleRunner:
         return n / dt, min(self.threads, n), f"{n} of {self.wl.T} tokens (seeded random subset), full top-k lists"
 
 
-def _kv_rows_for(wl, slots):
-    """kv row ids whose packed row lands in the given physical slots."""
-    if wl.kv_slot is None:
-        return slots
-    inv = np.empty(wl.num_slots, dtype=np.int64)
-    inv[wl.kv_slot] = np.arange(wl.num_slots)
-    return inv[slots]
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo; 'unknown' where neither names one)."""
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for line in r.stdout.splitlines():
+            k, _, v = line.partition(":")
+            if k.strip() == "Model name" and v.strip():
+                return v.strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                if k.strip() == "model name" and v.strip():
+                    return v.strip()
+    except OSError:
+        pass
+    import platform
+
+    return platform.machine() or "unknown"
+
+
+def measure(args, wl, rank, world, device, config=None):
+    """Times one workload (kernel-only and end to end) and returns its JSON line on rank 0."""
+    import torch
+
+    config = args.config if config is None else config
+    work = algorithmic_work(wl)
+    r = run_gpu(args, wl, rank, world, device, config)
+    if rank != 0:
+        return None
+    hbm, bf16, bf16_sus, peak_src = _peaks()
+    ms_per_step = r["total_ms"] / args.steps
+    value = job_value(world, wl.T, args.steps, r["total_ms"])
+    roof = roofline(work, ms_per_step / 1000.0, hbm, bf16)
+    roof.update({"traffic": _recorded_traffic(wl.name), "peak_source": peak_src,
+                 "algorithmic_bytes_per_launch": work["bytes"], "unique_bytes_per_launch": work["unique_bytes"],
+                 "flops_per_launch": work["flops"]})
+    # the same achieved figure against the GB300 nominal peaks (HBM3e 7.9 TB/s, dense bf16 2.25 PFLOP/s)
+    nominal = NOMINAL_HBM_GBS if roof["bound"] == "hbm" else NOMINAL_BF16_TFLOPS
+    roof["frac_of_nominal"] = roof["achieved"] / nominal
+    roof["nominal_peak"] = nominal
+    cpu_v, cores, sample = OracleRunner(wl).sample(args.cpu_seconds)
+    metric = METRIC if config == 3 else f"sparse-attn tokens/s ({wl.name})"
+    return {
+        "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(wl, work),
+        "roofline": roof,
+        "cpu_baseline": {"value": cpu_v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample,
+                         "cpu": cpu_model()},
+        "e2e": {"value": world * wl.T / (r["e2e_pipe_ms"] / 1000.0), "unit": "tokens/s", "h2d_bytes_per_step": r["h2d"],
+                "mode": "pipelined: step i+1's inputs copied in and step i-1's output read back while step i "
+                        "computes (two copy streams, two buffer sets), index sets rotating among 4",
+                "serial_value": world * wl.T / (r["e2e_ms"] / 1000.0),
+                "d2h_bytes_per_step": r["d2h"]},
+        "gpu_launches": args.steps * kernels_per_call(wl, torch.cuda.get_device_properties(device).multi_processor_count),
+        "clocks": r["clocks"],
+        "step_ms": {"median": statistics.median(r["times"]), "min": min(r["times"]), "max": max(r["times"])},
+    }
+
+
+def workload_config(wl, work):
+    return {"workload": wl.name, "tokens_per_step": wl.T, "heads": wl.H, "d_nope": wl.d_nope, "d_rope": wl.d_rope,
+            "d_v": wl.d_v, "topk": wl.topk, "valid_entries": work["n_valid"], "cache": "fp8_264B" if wl.kind else "bf16",
+            "slots": wl.num_slots, "page_size": wl.page_size or None,
+            "l2": f"{L2_FLUSH_BYTES >> 20} MB buffer written between timed steps (outside the events)"}
 
 
 def main():
@@ -478,6 +538,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--op", default="attn", choices=["attn", "requant"],
                     help="requant: time dsa_gather_requant on the decode workload's rows instead")
+    ap.add_argument("--no-prefill", dest="prefill", action="store_false",
+                    help="with the default decode workload, skip the second (T=8192 prefill) measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -488,12 +550,7 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     wl = W.config(args.config, seed=0)
-    work = algorithmic_work(wl)
-    metric = "sparse-attn tokens/s (256+0 FP8, T=256)" if args.config == 3 else f"sparse-attn tokens/s ({wl.name})"
-    cfg = {"workload": wl.name, "tokens_per_step": wl.T, "heads": wl.H, "d_nope": wl.d_nope, "d_rope": wl.d_rope,
-           "d_v": wl.d_v, "topk": wl.topk, "valid_entries": work["n_valid"], "cache": "fp8_264B" if wl.kind else "bf16",
-           "slots": wl.num_slots, "page_size": wl.page_size or None,
-           "l2": f"{L2_FLUSH_BYTES >> 20} MB buffer written between timed steps (outside the events)"}
+    metric = METRIC if args.config == 3 else f"sparse-attn tokens/s ({wl.name})"
 
     if args.impl == "reference":
         # The reference arm is the CPU oracle as it stands, on rank 0 only; each step runs a
@@ -517,8 +574,9 @@ def main():
         line = {"impl": "reference", "metric": metric, "value": v, "unit": "tokens/s", "n_gpus": 0,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * wl.T / v,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": cfg,
-                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+                "config": workload_config(wl, algorithmic_work(wl)),
+                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample,
+                                 "cpu": cpu_model()},
                 "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
@@ -540,34 +598,20 @@ def main():
         if world > 1:
             torch.distributed.destroy_process_group()
         return
-    r = run_gpu(args, wl, rank, world, device)
+    line = measure(args, wl, rank, world, device)
+    if args.config == 3 and args.prefill:
+        # the second headline workload, timed in the same run (every rank takes part in its
+        # barriers): BF16 causal prefill, T=8192
+        wl4 = W.config(4, seed=0)
+        sub = measure(args, wl4, rank, world, device, config=4)
+        if line is not None and sub is not None:
+            line["prefill"] = {k: sub[k] for k in ("metric", "value", "unit", "ms_per_step", "dtype", "config",
+                                                   "roofline", "cpu_baseline", "e2e", "gpu_launches", "clocks",
+                                                   "step_ms")}
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
         return
-    hbm, bf16, bf16_sus, peak_src = _peaks()
-    ms_per_step = r["total_ms"] / args.steps
-    value = job_value(world, wl.T, args.steps, r["total_ms"])
-    roof = roofline(work, ms_per_step / 1000.0, hbm, bf16)
-    roof.update({"traffic": _recorded_traffic(wl.name), "peak_source": peak_src,
-                 "algorithmic_bytes_per_launch": work["bytes"], "unique_bytes_per_launch": work["unique_bytes"],
-                 "flops_per_launch": work["flops"]})
-    cpu_v, cores, sample = OracleRunner(wl).sample(args.cpu_seconds)
-    line = {
-        "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
-        "roofline": roof,
-        "cpu_baseline": {"value": cpu_v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
-        "e2e": {"value": world * wl.T / (r["e2e_pipe_ms"] / 1000.0), "unit": "tokens/s", "h2d_bytes_per_step": r["h2d"],
-                "mode": "pipelined: step i+1's inputs copied in and step i-1's output read back while step i "
-                        "computes (two copy streams, two buffer sets), index sets rotating among 4",
-                "serial_value": world * wl.T / (r["e2e_ms"] / 1000.0),
-                "d2h_bytes_per_step": r["d2h"]},
-        "gpu_launches": args.steps * kernels_per_call(wl, torch.cuda.get_device_properties(device).multi_processor_count),
-        "clocks": r["clocks"],
-        "step_ms": {"median": statistics.median(r["times"]), "min": min(r["times"]), "max": max(r["times"])},
-    }
     print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -222,14 +222,19 @@ _WS = {}
 
 
 def _workspace(device, nbytes: int):
-    """A zero-filled workspace per device (the library leaves it zero-filled after every call)."""
+    """The default workspace of the current stream on ``device``: one zero-filled buffer per
+    (device, stream), so that calls on different streams, which may run at the same time on the
+    GPU, never share one (calls on one stream run in order, so they can). The library leaves a
+    workspace with no flag set after every call that completes without a timeout."""
     import torch
 
-    key = (device.index if device.index is not None else torch.cuda.current_device())
-    ws = _WS.get(key)
-    if ws is None or ws.numel() < nbytes:
-        ws = torch.zeros(nbytes, dtype=torch.uint8, device=device)
-        _WS[key] = ws
+    index = device.index if device.index is not None else torch.cuda.current_device()
+    key = (index, torch.cuda.current_stream(index).cuda_stream)
+    with _lock:
+        ws = _WS.get(key)
+        if ws is None or ws.numel() < nbytes:
+            ws = torch.zeros(nbytes, dtype=torch.uint8, device=torch.device("cuda", index))
+            _WS[key] = ws
     return ws
 
 
@@ -277,32 +282,56 @@ def dsa_sparse_attn_workspace_size(d_v: int = 256) -> int:
     return int(n.value)
 
 
-def dsa_sparse_attn(q, cache, kind: int, indices, sm_scale: float, *, d_nope: int = 256, d_rope: int = 0,
-                    d_v: int = None, block_table=None, page_size: int = 0, req_of_token=None, out=None, lse=None,
-                    workspace=None, error_word=None):
-    """Sparse MLA attention: out[t, h] = softmax_j(sm_scale * q[t,h].k_j) @ k_j[:d_v] over valid indices."""
+def _check_attn_inputs(q, cache, kind, indices, block_table, req_of_token, out, lse, error_word):
     import torch
 
-    d_v = d_nope if d_v is None else d_v
     _need_cuda("q", q, torch.bfloat16)
     _need_cuda("cache", cache, torch.uint8 if kind == CACHE_FP8_SCALED else torch.bfloat16)
     _need_cuda("indices", indices, torch.int32)
     _need_cuda("block_table", block_table, torch.int32)
     _need_cuda("req_of_token", req_of_token, torch.int32)
+    _need_cuda("out", out, torch.bfloat16)
     _need_cuda("lse", lse, torch.float32)
     _need_cuda("error_word", error_word, torch.int32)
+    for name, t in (("cache", cache), ("indices", indices), ("block_table", block_table),
+                    ("req_of_token", req_of_token), ("out", out), ("lse", lse), ("error_word", error_word)):
+        if t is not None and t.device != q.device:
+            raise ValueError(f"{name} is on {t.device}, q on {q.device}: every tensor must be on one device")
     if q.dim() != 3 or indices.dim() != 2:
         raise ValueError("q must be [T, H, D] and indices [T, topk]")
     if q.stride(2) != 1 or indices.stride(1) != 1:
         raise ValueError("q and indices must be contiguous along their last dimension")
+    if req_of_token is not None and not req_of_token.is_contiguous():
+        raise ValueError("req_of_token must be contiguous")
+    if lse is not None and not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous [T, H] tensor")
+
+
+def _prepare_attn(q, cache, kind, indices, d_v, block_table, req_of_token, out, lse, error_word):
+    import torch
+
     if kind == CACHE_BF16 and cache.dim() == 3:
         cache = cache.view(cache.shape[0], -1)
-    T = q.shape[0]
     if out is None:
-        out = torch.empty((T, q.shape[1], d_v), dtype=torch.bfloat16, device=q.device)
-    _need_cuda("out", out, torch.bfloat16)
+        out = torch.empty((q.shape[0], q.shape[1], d_v), dtype=torch.bfloat16, device=q.device)
+    _check_attn_inputs(q, cache, kind, indices, block_table, req_of_token, out, lse, error_word)
+    return cache, out
+
+
+def dsa_sparse_attn(q, cache, kind: int, indices, sm_scale: float, *, d_nope: int = 256, d_rope: int = 0,
+                    d_v: int = None, block_table=None, page_size: int = 0, req_of_token=None, out=None, lse=None,
+                    workspace=None, error_word=None):
+    """Sparse MLA attention: out[t, h] = softmax_j(sm_scale * q[t,h].k_j) @ k_j[:d_v] over valid indices.
+
+    Without ``workspace`` the call takes the default workspace of the current stream (one per
+    device and stream)."""
+    import torch
+
+    d_v = d_nope if d_v is None else d_v
+    cache, out = _prepare_attn(q, cache, kind, indices, d_v, block_table, req_of_token, out, lse, error_word)
     if workspace is None:
         workspace = _workspace(q.device, dsa_sparse_attn_workspace_size(d_v))
+    _need_cuda("workspace", workspace, torch.uint8)
     a = _attn_args(q, cache, kind, indices, sm_scale, d_nope, d_rope, d_v, block_table, page_size, req_of_token,
                    out, lse, workspace, error_word)
     _check(load_library().dsa_sparse_attn(ctypes.byref(a), _stream(q.device)), "dsa_sparse_attn")
@@ -312,18 +341,13 @@ def dsa_sparse_attn(q, cache, kind: int, indices, sm_scale: float, *, d_nope: in
 def dsa_sparse_attn_static_ws(q, cache, kind: int, indices, sm_scale: float, *, d_nope: int = 256, d_rope: int = 0,
                               d_v: int = None, block_table=None, page_size: int = 0, req_of_token=None, out=None,
                               lse=None, error_word=None):
-    """dsa_sparse_attn without a workspace: the library's built-in device scratch is used, so
-    nothing is allocated by the call (for callers that cannot allocate, e.g. while a CUDA graph
-    is being captured). The first call on a device must come before any stream capture."""
-    import torch
-
+    """dsa_sparse_attn without a workspace: the library's fixed device scratch is used, so the
+    call allocates no device memory (``out`` aside, when the caller passes none). For callers
+    that cannot allocate device memory when they call; the first call on a device does one-time
+    set-up and should come before any stream capture. Calls whose kernels may overlap on the GPU
+    share the one scratch array and race on it."""
     d_v = d_nope if d_v is None else d_v
-    _need_cuda("q", q, torch.bfloat16)
-    _need_cuda("indices", indices, torch.int32)
-    if kind == CACHE_BF16 and cache.dim() == 3:
-        cache = cache.view(cache.shape[0], -1)
-    if out is None:
-        out = torch.empty((q.shape[0], q.shape[1], d_v), dtype=torch.bfloat16, device=q.device)
+    cache, out = _prepare_attn(q, cache, kind, indices, d_v, block_table, req_of_token, out, lse, error_word)
     a = _attn_args(q, cache, kind, indices, sm_scale, d_nope, d_rope, d_v, block_table, page_size, req_of_token,
                    out, lse, None, error_word)
     _check(load_library().dsa_sparse_attn_static_ws(ctypes.byref(a), _stream(q.device)), "dsa_sparse_attn_static_ws")

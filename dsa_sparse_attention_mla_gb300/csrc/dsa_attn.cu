@@ -733,6 +733,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           }
           if (p.lse && dvh == 0 && hf == 0)
             p.lse[t * kHeads + h] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+          // every lane of this warp has read the parts: clear their publish flags, so that the
+          // workspace holds no set flag after the call (a later call that carries the same tag,
+          // such as a replay of a recorded launch, then never mistakes them for its own)
+          __syncwarp();
+          if (ok && lane == 0)
+            for (int k = 1; k <= nparts; ++k) p.flags[4 * (b + k) + sp] = 0;
 
         }
         tc_fence_before();
@@ -986,12 +992,6 @@ int next_attn_epoch(const void* workspace) {
 
 template <class C>
 static dsa_status_t launch(const dsa_attn_args_t* a, const DeviceInfo& dev, cudaStream_t stream) {
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(dsa_attn_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-  });
-  if (attr_err != cudaSuccess) return cuda_fail(attr_err);
   CUtensorMap tq;
   dsa_status_t st = encode_q_tensor_map(a, C::DK, &tq);
   if (st != DSA_OK) return st;
@@ -1043,6 +1043,23 @@ static dsa_status_t launch(const dsa_attn_args_t* a, const DeviceInfo& dev, cuda
 using CfgBf16_576 = AttnCfg<DSA_CACHE_BF16, 512, 64, 2, 64, 2>;
 using CfgFp8_576 = AttnCfg<DSA_CACHE_FP8_SCALED, 512, 64, 2, 64, 2>;
 
+dsa_status_t prepare_attn_kernels(int device) {
+  static std::mutex mu;
+  static bool done[64] = {};
+  if (device < 0 || device >= 64) return DSA_ERR_NO_DEVICE;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[device]) return DSA_OK;
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(dsa_attn_kernel<CfgBf16_576>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                CfgBf16_576::SMEM_BYTES)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(dsa_attn_kernel<CfgFp8_576>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                CfgFp8_576::SMEM_BYTES)) != cudaSuccess ||
+      (e = k128_set_attributes()) != cudaSuccess)
+    return cuda_fail(e);
+  done[device] = true;
+  return DSA_OK;
+}
+
 static dsa_status_t validate(const dsa_attn_args_t* a) {
   if (!a) return DSA_ERR_INVALID_ARGUMENT;
   if (a->T < 0 || a->num_slots < 0) return DSA_ERR_INVALID_ARGUMENT;
@@ -1051,7 +1068,8 @@ static dsa_status_t validate(const dsa_attn_args_t* a) {
   if (!((a->d_nope == 256 && a->d_rope == 0 && a->d_v == 256) || (a->d_nope == 512 && a->d_rope == 64 && a->d_v == 512)))
     return DSA_ERR_UNSUPPORTED;
   if (a->topk < 1 || a->topk > 16384) return DSA_ERR_INVALID_ARGUMENT;
-  if (!(a->sm_scale >= 0.0f) || !(a->sm_scale < 3.0e38f)) return DSA_ERR_INVALID_ARGUMENT;
+  // any finite scale (a negative one reverses the ranking of the keys; the pages set no limit)
+  if (!(a->sm_scale > -3.0e38f && a->sm_scale < 3.0e38f)) return DSA_ERR_INVALID_ARGUMENT;
   if (a->num_slots > 0x7FFFFFFELL) return DSA_ERR_UNSUPPORTED;
   if (a->T == 0) return DSA_OK;
   const int D = a->d_nope + a->d_rope;
@@ -1094,6 +1112,8 @@ dsa_status_t dsa_sparse_attn(const dsa_attn_args_t* a, void* stream) {
   st = current_device(&dev);
   if (st != DSA_OK) return st;
   if (a->workspace_bytes < attn_ws_bytes(dev.sm_count)) return DSA_ERR_WORKSPACE_TOO_SMALL;
+  st = prepare_attn_kernels(dev.device);
+  if (st != DSA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (a->d_nope == 256) return launch_attn_k128(a, dev, s);
   if (a->kind == DSA_CACHE_BF16) return launch<CfgBf16_576>(a, dev, s);
@@ -1103,13 +1123,13 @@ dsa_status_t dsa_sparse_attn(const dsa_attn_args_t* a, void* stream) {
 }  // extern "C"
 
 // ------------------------------------------------------------- fixed-scratch entry point --
-// Some callers cannot allocate device memory at call time: code running while a CUDA graph
-// is being captured on a stream (where cudaMalloc is not allowed), allocator-free runtimes and
-// embedded hosts that only hand the library input and output buffers. For them,
-// dsa_sparse_attn_static_ws takes its scratch (split-token partials and their flags) from
-// this file-scope device array instead of a caller-supplied workspace. It holds the partials
-// of at most kStaticWsCtas CTAs (about 10.6 MB); every GPU that loads the library keeps it
-// until the process exits.
+// Some callers cannot allocate device memory when they call the library: serving engines that
+// reserve all device memory up front for their KV page pool, runtimes that work from a fixed
+// memory plan, and latency-critical paths where an allocation could stall or synchronise the
+// device. For them, dsa_sparse_attn_static_ws takes its scratch (split-token partials, their
+// flags and the split bounds) from this file-scope device array instead of a caller-supplied
+// workspace. It holds the partials of at most kStaticWsCtas CTAs (about 10.6 MB); every GPU that
+// loads the library keeps it until the process exits.
 namespace dsa {
 constexpr int kStaticWsCtas = 160;
 constexpr size_t kStaticWsBytes = (size_t)kStaticWsCtas * kHeads * 256 * 4 + (size_t)kStaticWsCtas * 2 * kHeads * 4 +
@@ -1153,6 +1173,8 @@ extern "C" dsa_status_t dsa_sparse_attn_static_ws(const dsa_attn_args_t* a, void
   if (attn_ws_bytes(capped.sm_count) > kStaticWsBytes) return DSA_ERR_WORKSPACE_TOO_SMALL;
   void* ws = nullptr;
   st = static_ws_ptr(dev.device, &ws);
+  if (st != DSA_OK) return st;
+  st = prepare_attn_kernels(dev.device);
   if (st != DSA_OK) return st;
   b.workspace = ws;
   b.workspace_bytes = kStaticWsBytes;

@@ -31,6 +31,13 @@ struct AttnWorkspace {
 };
 AttnWorkspace attn_ws_layout(void* workspace, int sm_count);
 
+// One-time set-up, per device, of every attention kernel (the dynamic shared-memory limit is a
+// per-device attribute of each kernel). Every attention entry point runs it before its first
+// launch on a device; it does nothing on later calls.
+dsa_status_t prepare_attn_kernels(int device);
+// Sets the attributes of the keys-as-M kernels on the current device (part of the above).
+cudaError_t k128_set_attributes();
+
 // Keys-as-M kernel for the 256+0 latent geometry (dsa_attn_k128.cu).
 dsa_status_t launch_attn_k128(const dsa_attn_args_t* a, const DeviceInfo& dev, cudaStream_t stream);
 

@@ -936,6 +936,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (xsync(false) < 0) break;
+      // every softmax warp has read the parts: clear their publish flags, so that the workspace
+      // holds no set flag after the call (a later call that carries the same tag, such as a
+      // replay of a recorded launch, then never mistakes this call's flags for its own)
+      for (int f = sid; f < np * C::NSM; f += 32 * C::NSM) p.flags[8 * (b + 1 + f / C::NSM) + f % C::NSM] = 0;
       // copy out: 2048 16-byte granules (64 rows of 512 bytes), 8 per thread, row-contiguous
       {
         uint16_t* orow = p.out + t * p.out_st;
@@ -1281,12 +1285,6 @@ __global__ void __launch_bounds__(256) split_bounds_kernel(const int32_t* __rest
 template <int KIND>
 static dsa_status_t launch(const dsa_attn_args_t* a, const DeviceInfo& dev, cudaStream_t stream) {
   using C = Cfg<KIND>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(attn_k128_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-  });
-  if (attr_err != cudaSuccess) return cuda_fail(attr_err);
   CUtensorMap tq;
   dsa_status_t st = encode_q_tensor_map(a, kD, &tq);
   if (st != DSA_OK) return st;
@@ -1368,6 +1366,14 @@ static dsa_status_t launch(const dsa_attn_args_t* a, const DeviceInfo& dev, cuda
 }
 
 }  // namespace k128
+
+cudaError_t k128_set_attributes() {
+  cudaError_t e = cudaFuncSetAttribute(k128::attn_k128_kernel<DSA_CACHE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       k128::Cfg<DSA_CACHE_BF16>::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k128::attn_k128_kernel<DSA_CACHE_FP8_SCALED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              k128::Cfg<DSA_CACHE_FP8_SCALED>::SMEM_BYTES);
+}
 
 dsa_status_t launch_attn_k128(const dsa_attn_args_t* a, const DeviceInfo& dev, cudaStream_t stream) {
   if (a->kind == DSA_CACHE_BF16) return k128::launch<DSA_CACHE_BF16>(a, dev, stream);

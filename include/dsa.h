@@ -151,14 +151,17 @@ typedef struct dsa_attn_args {
   int64_t bt_stride;
   int page_size, max_pages;
   const int32_t* req_of_token;   /* int32 [T] request of each token, or NULL (request 0) */
-  float sm_scale;                /* softmax scale applied to q.k */
+  float sm_scale;                /* softmax scale applied to q.k: any finite value (0 gives the
+                                    mean of the valid rows, a negative value is allowed) */
   void* out;                     /* bf16 [T, H, d_v]; (t,h,d) at out + t*out_stride_t + h*out_stride_h + d */
   int64_t out_stride_t, out_stride_h;
   float* lse;                    /* optional fp32 [T, H] natural-log sum of exp(scores); NULL ok */
   void* workspace;               /* device scratch of dsa_sparse_attn_workspace_size bytes,
-                                    zero-filled before its first use in a process (the library
-                                    tags its flags with a per-workspace call counter, so it never
-                                    needs clearing again). One call at a time per workspace. */
+                                    zero-filled before its first use. A call tags the merge flags
+                                    it sets with a per-workspace counter and clears every flag it
+                                    consumes before it ends, so the workspace needs no clearing
+                                    between calls (zero-fill it again after a call that reported
+                                    DSA_DEVERR_TIMEOUT). One call at a time per workspace. */
   size_t workspace_bytes;
   int32_t* error_word;           /* optional device int32; DSA_DEVERR_* bits are OR-ed in */
 } dsa_attn_args_t;
@@ -188,26 +191,29 @@ DSA_API dsa_status_t dsa_sparse_attn(const dsa_attn_args_t* args, void* stream);
 
 /*
  * dsa_sparse_attn_static_ws - dsa_sparse_attn for callers that cannot allocate device memory.
- * (No counterpart on the pages: this is a deployment variant of the same computation.)
+ * (The pages have no counterpart: this is a deployment variant of the same computation.)
  *
- * Who needs it: code that enqueues work while a CUDA graph is being captured (cudaMalloc is
- * not allowed then), allocator-free runtimes, and hosts that hand the library only its input
- * and output buffers. Instead of args->workspace (ignored, together with workspace_bytes),
- * the split-token scratch lives in a fixed device array inside the library: about 10.6 MB,
- * enough for the partial results of up to 160 CTAs. Every GPU that loads the library holds
- * that array until the process exits. The call allocates nothing.
+ * Who needs it: callers that have no device allocator to offer, or may not use one when they
+ * call: serving engines that reserve all device memory up front for their KV page pool and
+ * hand libraries only input and output buffers, runtimes that work from a fixed memory plan,
+ * and latency-critical paths where an allocation could stall or synchronise the device. This
+ * entry point takes no workspace (args->workspace and workspace_bytes are ignored): its
+ * split-token scratch lives in a fixed device array inside the library, about 10.6 MB, enough
+ * for the partial results of up to 160 CTAs. Every GPU that loads the library holds that array
+ * until the process exits. The call allocates nothing.
  *
  * Arguments, results and errors are those of dsa_sparse_attn; the result is identical to
  * dsa_sparse_attn's on GPUs with at most 160 SMs. On a GPU with more SMs the kernel runs on 160
  * CTAs; if the array could not hold the scratch of the launch the call returns
  * DSA_ERR_WORKSPACE_TOO_SMALL without launching.
  *
- * The first call on each device looks up the array's device address (set-up that is not
- * allowed inside a stream capture): make that first call, per device, before capturing.
- * All calls share the one array (its flags are tagged with a per-call epoch, so nothing has to
- * be cleared between calls). Two calls whose kernels overlap on the GPU (different streams, no
- * ordering between them) race on it: order such calls, or use dsa_sparse_attn with separate
- * workspaces.
+ * The first call on each device does one-time set-up: it looks up the array's device address
+ * (cudaGetSymbolAddress) and sets the attention kernels' shared-memory limits on that device.
+ * Make that first call, per device, before any stream capture. All calls share the one array,
+ * which keeps what the last call left there: a call tags the flags it sets with a fresh value
+ * and clears every flag it consumes, so nothing has to be cleared between calls. Two calls
+ * whose kernels overlap on the GPU (different streams, no ordering between them) race on the
+ * array: order such calls, or use dsa_sparse_attn with separate workspaces.
  */
 DSA_API dsa_status_t dsa_sparse_attn_static_ws(const dsa_attn_args_t* args, void* stream);
 

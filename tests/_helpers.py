@@ -1,17 +1,25 @@
 """Shared helpers for the GPU parity tests: moving bit patterns between numpy and torch, building
 caches with the oracle, and the tolerance gates.
 
-Tolerances (attention): every element must satisfy |gpu - oracle| <= 2e-2 + 1e-2 * |oracle|
-(the bound stated for this path: max-abs 2e-2 and max-rel 1e-2 against the fp64 oracle on the
-same dequantised inputs), and in aggregate ||gpu - oracle||_F <= 1e-2 * ||oracle||_F, which a
-kernel with a dropped term or a wrong row would fail even where outputs are near zero.
+Tolerances (attention), every one enforced by check_close:
+  - elementwise |gpu - oracle| <= 2e-2 + 1e-2 * |oracle| (the bound stated for this path:
+    max-abs 2e-2 and max-rel 1e-2 against the fp64 oracle on the same dequantised inputs);
+  - max |gpu - oracle| <= 5e-3 for outputs of the workloads' scale (averages of hundreds of
+    unit-variance rows, a spread of about 0.04, where the observed error is about 1e-3): a wrong
+    row or a dropped term moves an output by far more. Tests whose outputs are of order one
+    (a single dominant key, large sm_scale) pass max_abs=2e-2, the literal bound, which their
+    bf16 output rounding alone (2^-9 relative) can approach;
+  - ||gpu - oracle||_F <= 1e-2 * ||oracle||_F, which a kernel with a dropped term or a wrong
+    row fails even where outputs are near zero.
 """
 import numpy as np
 import torch
 
 import oracle
+from oracle.workload_inputs import oracle_cache, slots_of_tokens  # noqa: F401 (re-exported)
 
-ATOL, RTOL, FRO = 2e-2, 1e-2, 1e-2
+ATOL, RTOL, FRO, MAX_ABS = 2e-2, 1e-2, 1e-2, 5e-3
+MAX_ABS_ORDER_ONE = 2e-2
 
 
 def bf16_dev(bits, device):
@@ -24,42 +32,6 @@ def bits_of(t):
 
 def f32_of(t):
     return t.detach().cpu().float().numpy()
-
-
-def oracle_cache(wl, rows=None):
-    """Host cache bytes for a workload, built by the oracle (uint8 rows for FP8, bf16 bits for BF16).
-
-    ``rows``: only these kv rows are generated and written (the rest stay zero) - enough for an
-    oracle run restricted to tokens whose entries name only those rows."""
-    if wl.kind == oracle.CACHE_BF16:
-        if rows is None:
-            return wl.kv.bits()
-        cache = np.zeros((wl.num_slots, wl.D), dtype=np.uint16)
-        cache[rows] = wl.kv.bits(rows)
-        return cache
-    src = wl.kv.bits() if rows is None else wl.kv.bits(rows)
-    if rows is None:
-        loc = wl.kv_slot
-    else:
-        loc = (wl.kv_slot[rows] if wl.kv_slot is not None else np.asarray(rows, dtype=np.int64))
-    rb = oracle.packed_row_bytes(wl.d_nope, wl.d_rope)
-    cache = np.zeros((wl.num_slots, rb), dtype=np.uint8)
-    return oracle.quant_k_cache(src[:, : wl.d_nope], src[:, wl.d_nope:] if wl.d_rope else None,
-                                out_loc=None if loc is None else np.asarray(loc, dtype=np.int64), cache=cache,
-                                num_slots=wl.num_slots)
-
-
-def slots_of_tokens(wl, tokens):
-    """Physical slots named by the valid entries of the given tokens."""
-    idx = wl.indices[tokens].astype(np.int64)
-    valid = idx >= 0
-    if wl.block_table is None:
-        s = idx[valid]
-    else:
-        r = wl.req_of_token[tokens][:, None].repeat(idx.shape[1], axis=1)[valid]
-        pos = idx[valid]
-        s = wl.block_table[r, pos // wl.page_size].astype(np.int64) * wl.page_size + pos % wl.page_size
-    return np.unique(s)
 
 
 def run_oracle(wl, cache, tokens=None, n_threads=0):
@@ -89,7 +61,7 @@ def run_oracle_on_dequantised(wl, cache, tokens=None, rows=None, n_threads=0):
                               req_of_token=wl.req_of_token, tokens=tokens, n_threads=n_threads)
 
 
-def check_close(gpu, ref, what=""):
+def check_close(gpu, ref, what="", max_abs=MAX_ABS):
     gpu = np.asarray(gpu, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert gpu.shape == ref.shape, (gpu.shape, ref.shape)
@@ -100,4 +72,22 @@ def check_close(gpu, ref, what=""):
     assert (err <= bound).all(), f"{what}: max err {err.max():.3e} at {worst} (ref {ref[worst]:.4f}, gpu {gpu[worst]:.4f})"
     fro = np.linalg.norm(gpu - ref) / max(np.linalg.norm(ref), 1e-30)
     assert fro <= FRO, f"{what}: relative Frobenius error {fro:.3e}"
-    return float(err.max()), float(fro)
+    emax = float(err.max()) if err.size else 0.0
+    print(f"[check_close] {what}: max abs err {emax:.3e}, rel Frobenius {fro:.3e}, |ref| max {np.abs(ref).max() if ref.size else 0:.3e}")
+    if max_abs is not None:
+        # a scalar, or one gate per token (first axis)
+        gate = np.asarray(max_abs, dtype=np.float64).reshape((-1,) + (1,) * (err.ndim - 1))
+        over = err - gate
+        arg = np.unravel_index(np.argmax(over), err.shape)
+        assert over.max() <= 0, (f"{what}: abs err {err[arg]:.3e} > {np.broadcast_to(gate, err.shape)[arg]:.1e} at "
+                                 f"{arg} (ref {ref[arg]:.4f})")
+    return emax, float(fro)
+
+
+def token_gates(indices, tokens=None, few=256):
+    """Per-token max-abs gates: MAX_ABS for tokens with at least ``few`` valid entries (outputs
+    are averages of many rows), MAX_ABS_ORDER_ONE for tokens with fewer (a causal prefix of a
+    handful of keys gives outputs of order one)."""
+    idx = indices if tokens is None else indices[tokens]
+    n = (idx >= 0).sum(axis=1)
+    return np.where(n >= few, MAX_ABS, MAX_ABS_ORDER_ONE)

@@ -85,7 +85,7 @@ def test_argument_errors_need_no_gpu(dsa_lib):
     a.q_stride_h, a.q_stride_t, a.idx_stride_t = 256, 64 * 256, 2048
     a.out_stride_h, a.out_stride_t = 256, 64 * 256
     good = dsa.DsaAttnArgs.from_buffer_copy(a)
-    for field, val, want in [("H", 32, 2), ("d_nope", 128, 2), ("topk", 0, 1), ("sm_scale", -1.0, 1),
+    for field, val, want in [("H", 32, 2), ("d_nope", 128, 2), ("topk", 0, 1), ("sm_scale", float("inf"), 1), ("sm_scale", float("nan"), 1),
                              ("q_stride_h", 100, 1), ("kind", 9, 1), ("out", 0, 1), ("T", -1, 1)]:
         b = dsa.DsaAttnArgs.from_buffer_copy(good)
         setattr(b, field, val)

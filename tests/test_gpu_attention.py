@@ -11,7 +11,8 @@ import torch
 import dsa_sparse_attention_mla_gb300 as dsa
 from dsa_sparse_attention_mla_gb300 import workloads as W
 
-from _helpers import bf16_dev, check_close, f32_of, oracle_cache, run_oracle, run_oracle_on_dequantised
+from _helpers import (MAX_ABS, MAX_ABS_ORDER_ONE, bf16_dev, check_close, f32_of, oracle_cache, run_oracle,
+                      run_oracle_on_dequantised, token_gates)
 
 pytestmark = pytest.mark.gpu
 
@@ -40,7 +41,7 @@ def _check_lse(got, ref, atol):
     np.testing.assert_allclose(got[fin], ref[fin], rtol=1e-5, atol=atol)
 
 
-def _check(wl, device, tokens=None, lse=True):
+def _check(wl, device, tokens=None, lse=True, max_abs=MAX_ABS):
     """Output and LSE against the oracle.
 
     BF16 cache: the oracle sees exactly the kernel's inputs (fp32 accumulation is the only
@@ -58,12 +59,12 @@ def _check(wl, device, tokens=None, lse=True):
     g_lse = None if not lse else (f32_of(lse_t) if tokens is None else f32_of(lse_t)[tokens])
     ref, ref_lse, bad = run_oracle(wl, cache, tokens=tokens)
     assert bad == 0
-    check_close(got, ref, wl.name + (" (exact dequantisation)" if wl.kind == 1 else ""))
+    check_close(got, ref, wl.name + (" (exact dequantisation)" if wl.kind == 1 else ""), max_abs=max_abs)
     if lse:
         _check_lse(g_lse, ref_lse, 2e-4)
     if wl.kind == 1 and wl.sm_scale <= 1.0 / np.sqrt(wl.D) + 1e-12:
         ref_d, ref_lse_d, _ = run_oracle_on_dequantised(wl, cache, tokens=tokens)
-        check_close(got, ref_d, wl.name + " (bf16-rounded dequantised rows)")
+        check_close(got, ref_d, wl.name + " (bf16-rounded dequantised rows)", max_abs=max_abs)
         if lse:
             _check_lse(g_lse, ref_lse_d, 2e-2)
     return out
@@ -133,10 +134,11 @@ def test_masked_single_duplicate_and_small_topk(gpu):
     idx[2, :] = 555
     idx[3, 5:] = -1
     idx[4, ::3] = -7
-    _check(wl, gpu)
+    # tokens 1 and 2 return one row (outputs of order one)
+    _check(wl, gpu, max_abs=MAX_ABS_ORDER_ONE)
     wl.kind = 1
     wl.kv_slot = None
-    _check(wl, gpu)
+    _check(wl, gpu, max_abs=MAX_ABS_ORDER_ONE)
 
 
 def test_single_entry_equals_row_bf16(gpu):
@@ -155,7 +157,8 @@ def test_repeated_pages_and_duplicates_paged(gpu):
     wl = W.fp8_paged(T=6, requests=2, positions=2048, page_size=64, topk=2048, n_valid=2000, seed=9, sm_scale=1 / 16)
     wl.block_table[1, :] = wl.block_table[1, 3]          # request 1: every logical page -> one physical page
     wl.indices[0, 1000:1500] = wl.indices[0, :500]        # duplicates are separate terms
-    _check(wl, gpu)
+    # request 1's tokens see only 64 distinct rows: outputs of order one
+    _check(wl, gpu, max_abs=np.where(wl.req_of_token == 1, MAX_ABS_ORDER_ONE, MAX_ABS))
 
 
 def test_out_of_range_entries_masked_and_flagged(gpu):
@@ -180,8 +183,20 @@ def test_large_scores_no_overflow(gpu):
     """Scale 1.0 on N(0,1) rows of width 256 gives scores of order 16-60: exercises the lazy
     rescale (running max growth above 2^8) and the max subtraction."""
     wl = W.bf16_direct(T=8, slots=4000, topk=2048, n_valid=2048, seed=12, sm_scale=1.0)
-    _check(wl, gpu)
+    _check(wl, gpu, max_abs=MAX_ABS_ORDER_ONE)
     wl = W.fp8_paged(T=8, requests=2, positions=2048, page_size=64, topk=2048, n_valid=2048, seed=13, sm_scale=0.5)
+    _check(wl, gpu, max_abs=MAX_ABS_ORDER_ONE)
+
+
+@pytest.mark.parametrize("kind", [0, 1])
+def test_negative_sm_scale(gpu, kind):
+    """A negative scale reverses the ranking of the keys (the softmax favours the keys least
+    aligned with q); any finite scale is accepted, as the pages set no limit."""
+    if kind == 0:
+        wl = W.bf16_direct(T=6, slots=4000, topk=2112, n_valid=2051, seed=17, sm_scale=-1 / 16, scatter_frac=0.2)
+    else:
+        wl = W.fp8_paged(T=6, requests=2, positions=4096, page_size=64, topk=2112, n_valid=2051, seed=18,
+                         sm_scale=-1 / 16, scatter_frac=0.2)
     _check(wl, gpu)
 
 
@@ -271,7 +286,10 @@ def test_fp8_large_scale_rows_among_ordinary_ones(gpu):
     out, lse_t = _gpu_attn(wl, cache, gpu, lse=True)
     ref, ref_lse, bad = run_oracle(wl, cache)
     assert bad == 0
-    check_close(f32_of(out), ref, "fp8 large-scale rows")
+    # the second output half holds values of order 2^15: compare it scaled back by that exact
+    # power of two, where the outputs are of order one
+    undo = np.concatenate([np.ones(128), np.full(128, 2.0 ** -15)])
+    check_close(f32_of(out) * undo, ref * undo, "fp8 large-scale rows", max_abs=MAX_ABS_ORDER_ONE)
     _check_lse(f32_of(lse_t), ref_lse, 2e-4)
 
 
@@ -284,7 +302,7 @@ def test_balanced_split_causal_prefill(gpu):
     rng = np.random.default_rng(5)
     tokens = np.unique(np.concatenate([np.arange(0, wl.T, 97), rng.integers(0, wl.T, 16),
                                        [0, 1, 127, 128, 2047, 2048, wl.T - 1]]))
-    out = _check(wl, gpu, tokens=tokens)
+    out = _check(wl, gpu, tokens=tokens, max_abs=token_gates(wl.indices, tokens))
     cache = oracle_cache(wl)
     again, _ = _gpu_attn(wl, cache, gpu)
     assert torch.equal(again.view(torch.int16), out.view(torch.int16))

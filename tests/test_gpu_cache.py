@@ -58,13 +58,20 @@ def test_quant_out_loc_strided_and_errors(gpu):
 
 def test_quant_every_e4m3_decision(gpu):
     """Rows whose quotients x/scale sweep every e4m3 rounding boundary: tiles of 128 values
-    with amax fixed at 448 * 2^k so that x / scale hits exact midpoints and their neighbours."""
+    with amax fixed at 448 * 2^k so that x / scale hits exact midpoints and the bf16 values one
+    bf16 step either side of each (the nearest inputs that do not tie), both signs."""
+    def bf16_step(v, d):  # the bf16 value d steps of the bf16 grid away from v (v is on the grid)
+        b = int(np.array([v], dtype=np.float32).view(np.uint32)[0]) >> 16
+        return float(np.array([(b + d) << 16], dtype=np.uint32).view(np.float32)[0])
+
     vals = []
     pos = sorted(set(abs(oracle.e4m3_value(c)) for c in range(0x7F)))
     for a, b in zip(pos[:-1], pos[1:]):
         mid = (a + b) / 2
-        vals += [mid, np.nextafter(np.float32(mid), np.float32(0)), np.nextafter(np.float32(mid), np.float32(500)),
-                 -mid, a, -b]
+        assert bf16_step(mid, 0) == mid  # every e4m3 midpoint is a bf16 value
+        below, above = bf16_step(mid, -1), bf16_step(mid, 1)
+        assert a < below < mid < above < b
+        vals += [mid, below, above, -mid, -below, -above, a, -b]
     vals = np.array(vals, dtype=np.float32)
     vals = vals[np.abs(vals) < 448]
     per = 127
@@ -152,7 +159,7 @@ def test_gather_requant_bit_exact(gpu, d_nope, d_rope):
                                  torch.from_numpy(idx).to(gpu)).cpu().numpy()
     diff = np.argwhere(got != ref)
     assert diff.size == 0, (len(diff), diff[:4].tolist(), got[tuple(diff[0])], ref[tuple(diff[0])],
-                            cache[idx[diff[0][0]], d_nope:d_nope + 4 * tiles].view(np.float32).tolist())
+                            cache[idx[diff[0][0]], d_nope:d_nope + 4 * (d_nope // 128)].view(np.float32).tolist())
 
 
 def test_gather_requant_paged_scatter_and_errors(gpu):
@@ -214,4 +221,4 @@ def test_gather_requant_non_canonical_rows_bit_exact(gpu, d_nope, d_rope):
                                  torch.from_numpy(idx).to(gpu)).cpu().numpy()
     diff = np.argwhere(got != ref)
     assert diff.size == 0, (len(diff), diff[:4].tolist(), got[tuple(diff[0])], ref[tuple(diff[0])],
-                            cache[idx[diff[0][0]], d_nope:d_nope + 4 * tiles].view(np.float32).tolist())
+                            cache[idx[diff[0][0]], d_nope:d_nope + 4 * (d_nope // 128)].view(np.float32).tolist())

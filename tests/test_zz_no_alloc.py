@@ -1,7 +1,8 @@
 """The fixed-scratch entry point dsa_sparse_attn_static_ws, called through the C ABI.
 
-It serves callers that cannot allocate device memory at call time (work enqueued during a
-CUDA graph capture, allocator-free hosts): the split-token scratch comes from a device array
+It serves callers that cannot allocate device memory when they call the library (engines that
+reserve all device memory up front, runtimes with a fixed memory plan, latency-critical paths
+where an allocation could stall the device): the split-token scratch comes from a device array
 inside the library. Two calls in a row must each match the workspace-taking dsa_sparse_attn
 within the attention tolerance of the other GPU tests (here they are in fact bit-identical:
 same grid, same schedule). The workload (8 tokens, top-k 2112) splits every token over several
