@@ -961,10 +961,12 @@ dsa_status_t encode_q_tensor_map(const dsa_attn_args_t* a, int dk, CUtensorMap* 
 static size_t attn_ws_split_bytes(int sm_count) { return ((size_t)(33 * sm_count + 1) * 8 + 255) & ~size_t(255); }
 
 size_t attn_ws_bytes(int sm_count) {
-  // partial o [G][64][256] fp32 + (max, sum) [G][2][64] fp32 + flags [G][8] int32 + the
-  // work-balanced split: entry counts of 32 unit slices per CTA and the G + 1 range bounds (int64)
+  // partial o [G][64][256] fp32 + up to four running values per head [G][4][64] fp32 (max and
+  // sum; the 8-bit-operand kernel adds one reference max per output half) + flags [G][8] int32
+  // + the work-balanced split: entry counts of 32 unit slices per CTA and the G + 1 range
+  // bounds (int64)
   const size_t o = (size_t)sm_count * kHeads * 256 * 4;
-  const size_t ml = (size_t)sm_count * 2 * kHeads * 4;
+  const size_t ml = (size_t)sm_count * 4 * kHeads * 4;
   const size_t fl = ((size_t)sm_count * 32 + 255) & ~size_t(255);
   return o + ml + fl + attn_ws_split_bytes(sm_count);
 }
@@ -975,8 +977,8 @@ AttnWorkspace attn_ws_layout(void* workspace, int sm_count) {
   AttnWorkspace r;
   r.o = reinterpret_cast<float*>(w);
   r.ml = reinterpret_cast<float*>(w + o_bytes);
-  r.flags = reinterpret_cast<int*>(w + o_bytes + (size_t)sm_count * 2 * kHeads * 4);
-  r.split = reinterpret_cast<int64_t*>(w + o_bytes + (size_t)sm_count * 2 * kHeads * 4 +
+  r.flags = reinterpret_cast<int*>(w + o_bytes + (size_t)sm_count * 4 * kHeads * 4);
+  r.split = reinterpret_cast<int64_t*>(w + o_bytes + (size_t)sm_count * 4 * kHeads * 4 +
                                        (((size_t)sm_count * 32 + 255) & ~size_t(255)));
   return r;
 }
@@ -1054,7 +1056,7 @@ dsa_status_t prepare_attn_kernels(int device) {
                                 CfgBf16_576::SMEM_BYTES)) != cudaSuccess ||
       (e = cudaFuncSetAttribute(dsa_attn_kernel<CfgFp8_576>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 CfgFp8_576::SMEM_BYTES)) != cudaSuccess ||
-      (e = k128_set_attributes()) != cudaSuccess)
+      (e = k128_set_attributes()) != cudaSuccess || (e = f8_set_attributes()) != cudaSuccess)
     return cuda_fail(e);
   done[device] = true;
   return DSA_OK;
@@ -1132,7 +1134,7 @@ dsa_status_t dsa_sparse_attn(const dsa_attn_args_t* a, void* stream) {
 // loads the library keeps it until the process exits.
 namespace dsa {
 constexpr int kStaticWsCtas = 160;
-constexpr size_t kStaticWsBytes = (size_t)kStaticWsCtas * kHeads * 256 * 4 + (size_t)kStaticWsCtas * 2 * kHeads * 4 +
+constexpr size_t kStaticWsBytes = (size_t)kStaticWsCtas * kHeads * 256 * 4 + (size_t)kStaticWsCtas * 4 * kHeads * 4 +
                                   (((size_t)kStaticWsCtas * 32 + 255) & ~size_t(255)) +
                                   (((size_t)(33 * kStaticWsCtas + 1) * 8 + 255) & ~size_t(255));
 static __device__ __align__(256) uint8_t g_static_ws[kStaticWsBytes];

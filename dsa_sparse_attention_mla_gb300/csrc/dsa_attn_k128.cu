@@ -1282,6 +1282,48 @@ __global__ void __launch_bounds__(256) split_bounds_kernel(const int32_t* __rest
   if (lane == 0) bounds[b] = bound;
 }
 
+}  // namespace k128
+
+dsa_status_t plan_unit_split(const dsa_attn_args_t* a, const DeviceInfo& dev, const AttnWorkspace& ws,
+                             cudaStream_t stream, UnitSplit* out) {
+  using namespace k128;
+  UnitSplit r;
+  r.NT = (a->topk + kBN - 1) / kBN;
+  r.U = a->T * (int64_t)r.NT;
+  // one persistent CTA per SM, with at least 4 units per CTA (small batches split each token
+  // into few parts), and few enough CTAs that a token spans at most kMaxParts + 1 of them
+  int64_t G = (r.U + 3) / 4;
+  if (G > dev.sm_count) G = dev.sm_count;
+  while (G > 1) {
+    const int64_t upc = r.U / G;  // fewest units any CTA holds
+    if ((r.NT + upc - 1) / upc + 1 <= kMaxParts + 1) break;
+    --G;
+  }
+  r.G = (int)G;
+  // Work-balanced split when CTAs hold many units (long, possibly uneven index lists): two small
+  // kernels on the same stream turn the lists into range bounds by work. Ranges keep at
+  // least ceil(NT / (kMaxParts - 1)) units, so that a token still spans at most kMaxParts CTAs.
+  r.bounds = nullptr;
+  r.gap = 1;
+  const int64_t gap = (r.NT + kMaxParts - 2) / (kMaxParts - 1);
+  if (r.G > 1 && r.G <= kSplitMaxCtas && r.U / r.G >= 64 && r.U >= (int64_t)r.G * gap) {
+    const int S = kSplitSlices * r.G;
+    int64_t* tot = ws.split;
+    int64_t* bnd = ws.split + S;
+    split_count_kernel<<<r.G, 1024, 0, stream>>>(a->indices, a->idx_stride_t, a->topk, r.NT, r.U, S, tot);
+    split_bounds_kernel<<<r.G + 1, 256, 0, stream>>>(a->indices, a->idx_stride_t, a->topk, r.NT, r.U, S, r.G, tot,
+                                                     bnd);
+    const cudaError_t le = cudaGetLastError();
+    if (le != cudaSuccess) return cuda_fail(le);
+    r.bounds = bnd;
+    r.gap = (int)gap;
+  }
+  *out = r;
+  return DSA_OK;
+}
+
+namespace k128 {
+
 template <int KIND>
 static dsa_status_t launch(const dsa_attn_args_t* a, const DeviceInfo& dev, cudaStream_t stream) {
   using C = Cfg<KIND>;
@@ -1321,35 +1363,14 @@ static dsa_status_t launch(const dsa_attn_args_t* a, const DeviceInfo& dev, cuda
   p.err = a->error_word;
   p.epoch = next_attn_epoch(a->workspace);
   p.T = a->T;
-  p.NT = (a->topk + kBN - 1) / kBN;
-  p.U = a->T * (int64_t)p.NT;
-  // one persistent CTA per SM, with at least 4 units per CTA (small batches split each token
-  // into few parts), and few enough CTAs that a token spans at most kMaxParts + 1 of them
-  int64_t G = (p.U + 3) / 4;
-  if (G > dev.sm_count) G = dev.sm_count;
-  while (G > 1) {
-    const int64_t upc = p.U / G;  // fewest units any CTA holds
-    if ((p.NT + upc - 1) / upc + 1 <= kMaxParts + 1) break;
-    --G;
-  }
-  p.G = (int)G;
-  // Work-balanced split when CTAs hold many units (long, possibly uneven index lists): two small
-  // kernels on the same stream turn the lists into range bounds by work. Ranges keep at
-  // least ceil(NT / (kMaxParts - 1)) units, so that a token still spans at most kMaxParts CTAs.
-  p.bounds = nullptr;
-  p.split_gap = 1;
-  const int64_t gap = (p.NT + kMaxParts - 2) / (kMaxParts - 1);
-  if (p.G > 1 && p.G <= kSplitMaxCtas && p.U / p.G >= 64 && p.U >= (int64_t)p.G * gap) {
-    const int S = kSplitSlices * p.G;
-    int64_t* tot = ws.split;
-    int64_t* bnd = ws.split + S;
-    split_count_kernel<<<p.G, 1024, 0, stream>>>(p.idx, p.idx_stride, p.topk, p.NT, p.U, S, tot);
-    split_bounds_kernel<<<p.G + 1, 256, 0, stream>>>(p.idx, p.idx_stride, p.topk, p.NT, p.U, S, p.G, tot, bnd);
-    const cudaError_t le = cudaGetLastError();
-    if (le != cudaSuccess) return cuda_fail(le);
-    p.bounds = bnd;
-    p.split_gap = (int)gap;
-  }
+  UnitSplit us;
+  st = plan_unit_split(a, dev, ws, stream, &us);
+  if (st != DSA_OK) return st;
+  p.NT = us.NT;
+  p.U = us.U;
+  p.G = us.G;
+  p.bounds = us.bounds;
+  p.split_gap = us.gap;
 
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)p.G);
@@ -1368,16 +1389,13 @@ static dsa_status_t launch(const dsa_attn_args_t* a, const DeviceInfo& dev, cuda
 }  // namespace k128
 
 cudaError_t k128_set_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(k128::attn_k128_kernel<DSA_CACHE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       k128::Cfg<DSA_CACHE_BF16>::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k128::attn_k128_kernel<DSA_CACHE_FP8_SCALED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              k128::Cfg<DSA_CACHE_FP8_SCALED>::SMEM_BYTES);
+  return cudaFuncSetAttribute(k128::attn_k128_kernel<DSA_CACHE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              k128::Cfg<DSA_CACHE_BF16>::SMEM_BYTES);
 }
 
 dsa_status_t launch_attn_k128(const dsa_attn_args_t* a, const DeviceInfo& dev, cudaStream_t stream) {
   if (a->kind == DSA_CACHE_BF16) return k128::launch<DSA_CACHE_BF16>(a, dev, stream);
-  return k128::launch<DSA_CACHE_FP8_SCALED>(a, dev, stream);
+  return launch_attn_f8(a, dev, stream);
 }
 
 }  // namespace dsa

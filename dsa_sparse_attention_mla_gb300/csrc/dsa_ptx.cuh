@@ -175,6 +175,34 @@ __device__ __forceinline__ void mma_bf16_lohi(uint32_t d_tmem, uint32_t a_lo, ui
       : "memory");
 }
 
+// Instruction descriptor, kind::f8f6f4 with e4m3 A/B and fp32 accumulation (A and B type
+// fields 0 = E4M3).
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, int a_mn_major, int b_mn_major) {
+  return (1u << 4) | ((uint32_t)a_mn_major << 15) | ((uint32_t)b_mn_major << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+// kind::f8f6f4 MMA (8-bit operands, K = 32 per instruction) with (low, high) descriptor words
+// and a compile-time accumulate flag, as mma_bf16_lohi.
+template <int ACC>
+__device__ __forceinline__ void mma_f8_lohi(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                            uint32_t b_hi, uint32_t idesc) {
+  asm volatile(
+      "{\n.reg .b64 da, db;\n.reg .pred p;\nmov.b64 da, {%1, %2};\nmov.b64 db, {%3, %4};\n"
+      "setp.ne.b32 p, %6, 0;\ntcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %5, p;\n}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "n"(ACC)
+      : "memory");
+}
+// The same with a run-time accumulate flag.
+__device__ __forceinline__ void mma_f8_lohi_rt(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                               uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .b64 da, db;\n.reg .pred p;\nmov.b64 da, {%1, %2};\nmov.b64 db, {%3, %4};\n"
+      "setp.ne.b32 p, %6, 0;\ntcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %5, p;\n}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive (once) on an mbarrier when all previously issued tcgen05 MMAs of this thread complete.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)

@@ -181,11 +181,14 @@ DSA_API dsa_status_t dsa_sparse_attn_workspace_size(const dsa_attn_args_t* args,
  *   lse[t,h] = log(sum_j exp(s_j)). A token with no valid entry gets out = 0 and lse = -inf.
  * Duplicate indices are separate terms. The result is bit-identical across repeated calls with
  * the same inputs on the same device.
- * Arithmetic: products of bf16 operands accumulated in fp32 (tensor cores); probabilities enter
- * the value product as bf16. 256+0 FP8 rows: the e4m3 codes enter the tensor core exactly and
- * the fp32 tile scales multiply the score and probability accumulators, i.e. the keys are the
- * exact products code * scale (never rounded to bf16). 512+64 FP8 rows: keys are
- * bf16_rne(code * scale), the rows dsa_gather_dequant returns.
+ * Arithmetic. BF16 rows: products of bf16 operands accumulated in fp32 (tensor cores);
+ * probabilities enter the value product as bf16. 256+0 FP8 rows: 8-bit tensor-core products
+ * accumulated in fp32; the e4m3 codes enter exactly, the bf16 query as two e4m3 terms per head
+ * and 128-column tile (a power-of-two scale each; exact for every component within 2^9 of the
+ * tile's largest), the fp32 tile scales multiply the score accumulators, and the probabilities
+ * (times each key's tile scale) enter the value product as two e4m3 terms, 8 significant bits.
+ * The keys are thus the exact products code * scale (never rounded to bf16). 512+64 FP8 rows:
+ * keys are bf16_rne(code * scale), the rows dsa_gather_dequant returns.
  */
 DSA_API dsa_status_t dsa_sparse_attn(const dsa_attn_args_t* args, void* stream);
 
