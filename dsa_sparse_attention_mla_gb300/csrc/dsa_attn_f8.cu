@@ -25,15 +25,15 @@
 //    c = sm_scale * log2(e). Three running maxima per head: m of x, for the row sums of
 //    p = 2^(x - m), and m'_t of x + log2 sc_t, the reference of output half t (columns
 //    128t .. 128t + 127, scale tile t). The weights of the output product,
-//    P_t = p * sc_t * 2^(m - m'_t + 5) = 2^(x + log2 sc_t - m'_t + 5), are proportional to the
-//    size of each key's contribution to that half, so they stay in e4m3 range (below 2^8)
-//    whatever the scales are, with the largest near 2^5. P_t is written as two e4m3 terms
+//    P_t = p * sc_t * 2^(m - m'_t + 4) = 2^(x + log2 sc_t - m'_t + 4), are proportional to the
+//    size of each key's contribution to that half, so they stay in e4m3 range (below 2^8.5)
+//    whatever the scales are, with the largest near 2^4. P_t is written as two e4m3 terms
 //    (hi: P_t truncated to four significant bits, lo: the rest rounded), 8 significant bits in
 //    all, each key's two 64-head rows side by side (128 bytes per key and half). Two P buffers,
 //    so that the pass of tile g + 1 runs while the output product of tile g reads its P.
 //  * Output O^T += V^T P^T in two M = 128 halves of d_v (V^T read MN-major from the same 8-bit
 //    tile, one half per scale tile), N = 64 heads, the hi and lo terms of P into the same
-//    accumulator. Half t is normalised by 2^(m'_t - m - 5) / l at the token's end.
+//    accumulator. Half t is normalised by 2^(m'_t - m - 4) / l at the token's end.
 //  * Persistent cooperative launch, one CTA per SM; (token, 128-position tile) units split into
 //    contiguous ranges per CTA; a token cut by a range boundary is merged in-kernel by the CTA
 //    holding its first tiles (fixed order, no atomics on data).
@@ -66,10 +66,10 @@ constexpr int kPBUF = 2;        // P buffers
 constexpr int kMaxParts = 16;   // most parts of one split token (the launch guarantees it)
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kSplitMaxCtas = 192;
-constexpr float kTau = 3.0f;     // lazy maxima of the output halves: a tile may exceed them by 2^3
+constexpr float kTau = 4.5f;     // lazy maxima of the output halves: a tile may exceed them by 2^4.5
 constexpr float kTauL = 20.0f;   // lazy maximum of the row sums (fp32 sums: a wide margin is safe)
-constexpr int kPShift = 5;       // P weights carry an extra 2^5: the largest is about 2^5 ...
-constexpr float kPMax = 288.0f;  // ... and at most 2^(3 + 5) = 256 (with margin; e4m3 tops at 448)
+constexpr int kPShift = 4;       // P weights carry an extra 2^4: the largest is about 2^4 ...
+constexpr float kPMax = 400.0f;  // ... and at most 2^(4.5 + 4) = 362 (with margin; e4m3 tops at 448)
 
 // shared memory carve-up (offsets from a 1024-aligned base)
 constexpr int Q_OFF = 0;                // Q: [hi chunk 0 | hi chunk 1 | lo 0 | lo 1], 8 KB each
