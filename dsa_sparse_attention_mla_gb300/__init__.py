@@ -22,7 +22,7 @@ __all__ = [
     "DsaError", "CACHE_BF16", "CACHE_FP8_SCALED", "DEVERR_INDEX_OUT_OF_RANGE", "DEVERR_TIMEOUT",
     "DEVERR_SLOT_OUT_OF_RANGE", "library_path", "load_library", "dsa_status_string",
     "dsa_packed_row_bytes", "dsa_cache_row_bytes", "dsa_quant_k_cache", "dsa_gather_dequant", "dsa_gather_requant",
-    "dsa_sparse_attn_workspace_size", "dsa_sparse_attn", "dsa_sparse_attn_static_ws", "DsaAttnArgs",
+    "dsa_sparse_attn_workspace_size", "dsa_sparse_attn", "dsa_sparse_attn_static_ws", "dsa_topk_select", "DsaAttnArgs",
 ]
 
 CACHE_BF16 = 0
@@ -95,6 +95,8 @@ def load_library():
         lib.dsa_sparse_attn.restype = i32
         lib.dsa_sparse_attn_static_ws.argtypes = [ctypes.POINTER(DsaAttnArgs), P]
         lib.dsa_sparse_attn_static_ws.restype = i32
+        lib.dsa_topk_select.argtypes = [P, i64, i64, i64, P, i32, P, i64, P]
+        lib.dsa_topk_select.restype = i32
         _LIB = lib
         return lib
 
@@ -351,4 +353,29 @@ def dsa_sparse_attn_static_ws(q, cache, kind: int, indices, sm_scale: float, *, 
     a = _attn_args(q, cache, kind, indices, sm_scale, d_nope, d_rope, d_v, block_table, page_size, req_of_token,
                    out, lse, None, error_word)
     _check(load_library().dsa_sparse_attn_static_ws(ctypes.byref(a), _stream(q.device)), "dsa_sparse_attn_static_ws")
+    return out
+
+
+def dsa_topk_select(scores, K: int, *, lengths=None, out=None):
+    """int32 [T, K]: per row, the positions of its K largest scores (ties: lower position first),
+    in that order, then -1 (positions at or past lengths[t] are not considered)."""
+    import torch
+
+    _need_cuda("scores", scores, torch.float32)
+    _need_cuda("lengths", lengths, torch.int32)
+    if scores.dim() != 2 or scores.stride(1) != 1:
+        raise ValueError("scores must be [T, S], contiguous along S")
+    T, S = scores.shape
+    if out is None:
+        out = torch.empty((T, K), dtype=torch.int32, device=scores.device)
+    _need_cuda("out", out, torch.int32)
+    if out.dim() != 2 or out.shape[0] != T or out.shape[1] < K or out.stride(1) != 1:
+        raise ValueError("out must be [T, >=K] int32, contiguous along its last dimension")
+    if lengths is not None:
+        lengths = lengths.contiguous()
+        if lengths.numel() != T:
+            raise ValueError("lengths must have one entry per row")
+    st = load_library().dsa_topk_select(_ptr(scores), T, S, scores.stride(0), _ptr(lengths), int(K), _ptr(out),
+                                        out.stride(0), _stream(scores.device))
+    _check(st, "dsa_topk_select")
     return out

@@ -132,6 +132,28 @@ DSA_API dsa_status_t dsa_gather_requant(const void* cache, int64_t num_slots, in
                                 const int32_t* req_of_index, const int64_t* out_loc, void* out,
                                 int64_t out_slots, int32_t* error_word, void* stream);
 
+/*
+ * dsa_topk_select - the top-k position list of each query token from its index-logits, the
+ * input dsa_sparse_attn gathers by (FreeToken PR #270 "glm5_next: support GLM-5.3-Flash",
+ * Summary, the DSA key-pooling bullet: pooled keys are scored and the best-scoring positions
+ * read; PR #38547, Direct GLM geometry coverage list: top-k widths 2048 and 2112, lists padded
+ * with -1). The pages give the scoring itself no formula: the scores are an input.
+ *   scores        fp32 [T, S], row t at scores + t * score_stride_t (stride >= S); finite or
+ *                 +-inf (NaN is outside the contract); may be NULL when S == 0
+ *   lengths       int32 [T] positions each row considers (0 .. n_t - 1, n_t = lengths[t]
+ *                 clamped to [0, S]: a causal limit), or NULL (n_t = S)
+ *   K             result width, 1 .. 16384
+ *   indices       int32 [T, K] at indices + t * idx_stride_t (stride >= K): the positions of the
+ *                 min(K, n_t) largest scores of row t in descending score order, equal scores
+ *                 in ascending position order (-0.0 equals +0.0), then -1 up to K
+ * The result depends only on the inputs (integer decisions on order-preserving keys). T == 0 is
+ * a no-op; errors: DSA_ERR_INVALID_ARGUMENT (sizes, strides, null or misaligned pointers),
+ * DSA_ERR_UNSUPPORTED (S above 2^31 - 1).
+ */
+DSA_API dsa_status_t dsa_topk_select(const float* scores, int64_t T, int64_t S, int64_t score_stride_t,
+                             const int32_t* lengths, int K, int32_t* indices, int64_t idx_stride_t,
+                             void* stream);
+
 /* Arguments of dsa_sparse_attn. Zero-initialise, then fill. */
 typedef struct dsa_attn_args {
   const void* q;                 /* bf16 [T, H, d_nope + d_rope]; element (t,h,d) at

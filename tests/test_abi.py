@@ -20,6 +20,7 @@ def _declared():
 def test_header_declares_the_entry_points():
     names = _declared()
     for n in ["dsa_quant_k_cache", "dsa_gather_dequant", "dsa_gather_requant", "dsa_sparse_attn", "dsa_sparse_attn_workspace_size",
+              "dsa_topk_select",
               "dsa_packed_row_bytes", "dsa_cache_row_bytes", "dsa_status_string", "dsa_last_cuda_error"]:
         assert n in names
 
@@ -78,6 +79,14 @@ def test_argument_errors_need_no_gpu(dsa_lib):
                                 None, None) == 1  # more results than output rows, no out_loc
     assert L.dsa_gather_requant(fake, i64(10), 256, 0, fake, i64(0), None, i64(0), 0, 0, None, None, fake, i64(10),
                                 None, None) == 0
+    # top-k selection: bad width, bad stride, missing pointer; nothing to do
+    assert L.dsa_topk_select(fake, i64(4), i64(100), i64(100), None, 0, fake, i64(8), None) == 1
+    assert L.dsa_topk_select(fake, i64(4), i64(100), i64(100), None, 16385, fake, i64(16385), None) == 1
+    assert L.dsa_topk_select(fake, i64(4), i64(100), i64(99), None, 8, fake, i64(8), None) == 1
+    assert L.dsa_topk_select(fake, i64(4), i64(100), i64(100), None, 8, fake, i64(7), None) == 1
+    assert L.dsa_topk_select(None, i64(4), i64(100), i64(100), None, 8, fake, i64(8), None) == 1
+    assert L.dsa_topk_select(fake, i64(4), i64(1 << 31), i64(1 << 31), None, 8, fake, i64(8), None) == 2
+    assert L.dsa_topk_select(fake, i64(0), i64(100), i64(100), None, 8, fake, i64(8), None) == 0
     a = dsa.DsaAttnArgs()
     a.H, a.d_nope, a.d_rope, a.d_v, a.topk, a.T = 64, 256, 0, 256, 2048, 4
     a.q = a.cache = a.indices = a.out = a.workspace = 0x10000
