@@ -94,7 +94,8 @@ constexpr int BAR_OFF = SPLIT_OFF + 8 * (kSplitMaxCtas + 1);
 enum : int {
   B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_KEMPTY = B_KFULL + kKST, B_MFULL = B_KEMPTY + kKST,
   B_MEMPTY = B_MFULL + kMST, B_SFULL = B_MEMPTY + kMST, B_SEMPTY = B_SFULL + 2, B_PFULL = B_SEMPTY + 2,
-  B_PVDONE = B_PFULL + kPBUF, B_XBAR = B_PVDONE + 2, B_DRAIN = B_XBAR + 1, B_RANGE = B_DRAIN + 2, NBARS = B_RANGE + 1
+  B_PVDONE = B_PFULL + kPBUF, B_XBAR = B_PVDONE + 2, B_DRAIN = B_XBAR + 1, B_RANGE = B_DRAIN + 2, B_MERGE = B_RANGE + 1,
+  NBARS = B_MERGE + 3
 };
 constexpr int MISC_OFF = BAR_OFF + 8 * NBARS;
 constexpr int SMEM_BYTES = MISC_OFF + 32 + 1024;  // + alignment slack
@@ -266,6 +267,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_f8_kernel(const __grid_const
   const uint32_t xbar = bar(B_XBAR);        // softmax-warp exchange
   const uint32_t mma_drain = bar(B_DRAIN);  // every MMA of an issuer complete (+0: scores, +8: output)
   const uint32_t range_ready = bar(B_RANGE);
+  // a head's merge: the other parts' (m, l, m'_0, m'_1) rows (+0) and their O^T halves, two
+  // parts in flight (+1, +2)
+  auto merge_bar = [&](int i) { return bar(B_MERGE + i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + MISC_OFF + 4);
   int64_t* range = reinterpret_cast<int64_t*>(smem + MISC_OFF + 8);  // this CTA's units [u0, u1)
@@ -293,6 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_f8_kernel(const __grid_const
     mbar_init(mma_drain, 1);
     mbar_init(mma_drain + 8, 1);
     mbar_init(range_ready, 1);
+    for (int i = 0; i < 3; ++i) mbar_init(merge_bar(i), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -938,8 +943,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_f8_kernel(const __grid_const
           wsml[((int64_t)b * 4 + 3) * kH + sid] = mh1;
         }
         if (had) {
-          float* w0 = p.ws_o + ((int64_t)b * kD + tr) * kH + hb;
-          float* w1 = p.ws_o + ((int64_t)b * kD + 128 + tr) * kH + hb;
+          // rows dv = tr and 128 + tr of O^T; the 16-byte granule of heads 4q .. 4q + 3 sits at
+          // position q ^ (tr & 15) of its 256-byte row, so that the merge reads the rows from
+          // shared memory without bank conflicts
+          float* w0 = p.ws_o + ((int64_t)b * kD + tr) * kH;
+          float* w1 = p.ws_o + ((int64_t)b * kD + 128 + tr) * kH;
 #pragma unroll 1
           for (int ch = 0; ch < 2; ++ch) {
             uint32_t o0[16], o1[16];
@@ -948,8 +956,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_f8_kernel(const __grid_const
             tc_wait_ld();
 #pragma unroll
             for (int i = 0; i < 16; i += 4) {
-              *reinterpret_cast<float4*>(w0 + 16 * ch + i) = make_float4(u2f(o0[i]), u2f(o0[i + 1]), u2f(o0[i + 2]), u2f(o0[i + 3]));
-              *reinterpret_cast<float4*>(w1 + 16 * ch + i) = make_float4(u2f(o1[i]), u2f(o1[i + 1]), u2f(o1[i + 2]), u2f(o1[i + 3]));
+              const int pos = 4 * ((((hb + 16 * ch + i) >> 2) ^ tr) & 15);
+              *reinterpret_cast<float4*>(w0 + pos) = make_float4(u2f(o0[i]), u2f(o0[i + 1]), u2f(o0[i + 2]), u2f(o0[i + 3]));
+              *reinterpret_cast<float4*>(w1 + pos) = make_float4(u2f(o1[i]), u2f(o1[i + 1]), u2f(o1[i + 2]), u2f(o1[i + 3]));
             }
           }
         }
@@ -982,15 +991,42 @@ __global__ void __launch_bounds__(kThreads, 1) attn_f8_kernel(const __grid_const
       __syncwarp();
       if (!okp) fail(DSA_DEVERR_TIMEOUT);
       const int np = (okp && nparts <= kMaxParts) ? nparts : 0;
+      // The parts' rows come into shared memory by bulk copies: their (m, l, m'_0, m'_1) rows
+      // (consecutive workspace slots b+1 .. b+np) into the Q buffer, and their O^T halves into
+      // two slot pairs (K stages 0-1, and K stage 2 with P buffer 1), two parts in flight. A
+      // head segment is its CTA's last, so none of these buffers is in use any more: every
+      // output product is complete, and no further query split or row load follows.
+      auto slot = [&](int pair, int half) -> uint32_t {
+        return sbase + (pair == 0 ? KT_OFF + half * KT_BYTES : (half == 0 ? KT_OFF + 2 * KT_BYTES : P_OFF + P_BYTES));
+      };
+      auto fetch_part = [&](int u) {  // one thread: fill u = part u % np + 1 into slot pair u & 1
+        const uint32_t mb = merge_bar(1 + (u & 1));
+        const float* src = p.ws_o + (int64_t)(b + 1 + u % np) * kD * kH;
+        mbar_arrive_expect_tx(mb, kD * kH * 4);
+        bulk_g2s(slot(u & 1, 0), src, 128 * kH * 4, mb);
+        bulk_g2s(slot(u & 1, 1), src + 128 * kH, 128 * kH * 4, mb);
+      };
+      if (np > 0 && sid == 0) {
+        // the flags were acquired by this warp; order the parts' data (read by the async proxy)
+        // after them, and the buffers' earlier uses before the copies
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(merge_bar(0), np * 4 * kH * 4);
+        bulk_g2s(sbase + Q_OFF, wsml + (int64_t)(b + 1) * 4 * kH, np * 4 * kH * 4, merge_bar(0));
+        fetch_part(0);
+        if (np >= 2) fetch_part(1);
+      }
       if (sid < kH) {
         // sums relative to the largest m over the parts; each half's O of each part weighted
         // by 2^(m'_t - M - kPShift) / L
+        const float* pml = reinterpret_cast<const float*>(smem + Q_OFF);  // [np][4][64]
+        if (np > 0 && !mbar_wait(merge_bar(0), 0, kWaitNs)) fail(DSA_DEVERR_TIMEOUT);
         float M = mrow;
-        for (int k = 1; k <= np; ++k) M = fmaxf(M, wsml[((int64_t)(b + k) * 4 + 0) * kH + sid]);
+        for (int k = 1; k <= np; ++k) M = fmaxf(M, pml[(k - 1) * 4 * kH + sid]);
         float L = lsum > 0.0f ? exp2f(mrow - M) * lsum : 0.0f;
         for (int k = 1; k <= np; ++k) {
-          const float mk = wsml[((int64_t)(b + k) * 4 + 0) * kH + sid];
-          const float lk = wsml[((int64_t)(b + k) * 4 + 1) * kH + sid];
+          const float mk = pml[((k - 1) * 4 + 0) * kH + sid];
+          const float lk = pml[((k - 1) * 4 + 1) * kH + sid];
           if (lk > 0.0f) L += exp2f(mk - M) * lk;
         }
         const float inv = L > 0.0f ? 1.0f / L : 0.0f;
@@ -998,20 +1034,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_f8_kernel(const __grid_const
         red_al[sid] = lsum > 0.0f ? exp2f(mh0 - base) * inv : 0.0f;
         red_al[kH + sid] = lsum > 0.0f ? exp2f(mh1 - base) * inv : 0.0f;
         for (int k = 1; k <= np; ++k) {
-          const bool live = wsml[((int64_t)(b + k) * 4 + 1) * kH + sid] > 0.0f;
-          red_wk[(k - 1) * kH + sid] = live ? exp2f(wsml[((int64_t)(b + k) * 4 + 2) * kH + sid] - base) * inv : 0.0f;
-          red_wk[(kMaxParts + k - 1) * kH + sid] =
-              live ? exp2f(wsml[((int64_t)(b + k) * 4 + 3) * kH + sid] - base) * inv : 0.0f;
+          const bool live = pml[((k - 1) * 4 + 1) * kH + sid] > 0.0f;
+          red_wk[(k - 1) * kH + sid] = live ? exp2f(pml[((k - 1) * 4 + 2) * kH + sid] - base) * inv : 0.0f;
+          red_wk[(kMaxParts + k - 1) * kH + sid] = live ? exp2f(pml[((k - 1) * 4 + 3) * kH + sid] - base) * inv : 0.0f;
         }
         if (p.lse) p.lse[t * kH + sid] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
       }
       if (xsync(false) < 0) break;
-      // combine and stage the bf16 block [64 heads][256 columns] in a P buffer (both idle: every
-      // output product of this segment is complete)
+      // combine: this CTA's O (TMEM) and the parts in order, then stage the bf16 block
+      // [64 heads][256 columns] in P buffer 0 (idle: every output product is complete)
       uint16_t* stage = reinterpret_cast<uint16_t*>(smem + P_OFF);
+      // One 16-head chunk at a time (32 accumulators): the parts stream through the two slot
+      // pairs in order, and with more than two parts the second chunk fetches them again.
+      bool okm = true;
+      int uses = 0;  // slot-pair fills consumed so far (fill u is part (u % np) + 1 in pair u & 1)
 #pragma unroll 1
-      for (int ch = 0; ch < 2; ++ch) {
+      for (int ch = 0; ch < 2 && okm; ++ch) {
         const int h0 = hb + 16 * ch;
+        if (np <= 2) uses = 0;  // both parts stay in their slot pairs for the second chunk
         float acc0[16], acc1[16];
         if (had) {
           uint32_t o0[16], o1[16];
@@ -1027,15 +1067,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_f8_kernel(const __grid_const
 #pragma unroll
           for (int i = 0; i < 16; ++i) acc0[i] = acc1[i] = 0.0f;
         }
-        for (int k = 1; k <= np; ++k) {
+        for (int k = 1; k <= np; ++k, ++uses) {
+          const int pr = uses & 1;
+          if (!wait_all(mbar_wait(merge_bar(1 + pr), (uses >> 1) & 1, kWaitNs))) {
+            okm = false;
+            break;
+          }
+          const uint8_t* r0 = smem + (slot(pr, 0) - sbase) + tr * 256;
+          const uint8_t* r1 = smem + (slot(pr, 1) - sbase) + tr * 256;
           const float* wk0 = red_wk + (k - 1) * kH + h0;
           const float* wk1 = red_wk + (kMaxParts + k - 1) * kH + h0;
-          const float* s0 = p.ws_o + ((int64_t)(b + k) * kD + tr) * kH + h0;
-          const float* s1 = p.ws_o + ((int64_t)(b + k) * kD + 128 + tr) * kH + h0;
 #pragma unroll
           for (int i = 0; i < 16; i += 4) {
-            const float4 x = *reinterpret_cast<const float4*>(s0 + i);
-            const float4 y = *reinterpret_cast<const float4*>(s1 + i);
+            const int pos = 16 * ((((h0 + i) >> 2) ^ tr) & 15);
+            const float4 x = *reinterpret_cast<const float4*>(r0 + pos);
+            const float4 y = *reinterpret_cast<const float4*>(r1 + pos);
             acc0[i] += wk0[i] * x.x;
             acc0[i + 1] += wk0[i + 1] * x.y;
             acc0[i + 2] += wk0[i + 2] * x.z;
@@ -1045,13 +1091,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_f8_kernel(const __grid_const
             acc1[i + 2] += wk1[i + 2] * y.z;
             acc1[i + 3] += wk1[i + 3] * y.w;
           }
+          // the fill two ahead: the next part of this chunk's pass, or of the second chunk's
+          const int ahead = uses + 2, total = np > 2 ? 2 * np : np;
+          if (ahead < total) {
+            // every warp has read this slot pair: refill it
+            if (xsync(false) < 0) {
+              okm = false;
+              break;
+            }
+            if (sid == 0) {
+              fence_proxy_async_smem();
+              fetch_part(ahead);
+            }
+          }
         }
+        if (!okm) break;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           stage[(h0 + i) * kD + tr] = __bfloat16_as_ushort(__float2bfloat16_rn(acc0[i]));
           stage[(h0 + i) * kD + 128 + tr] = __bfloat16_as_ushort(__float2bfloat16_rn(acc1[i]));
         }
       }
+      if (!okm) break;
       if (xsync(false) < 0) break;
       // every softmax warp has read the parts: clear their publish flags, so that the workspace
       // holds no set flag after the call (a later call that carries the same tag, such as a

@@ -107,7 +107,7 @@ struct Cfg {
   static constexpr int RED_FLOATS = 8 * kH + kMaxParts * kH + 2 * NSM;
   static constexpr int SPLIT_OFF = RED_OFF + ((RED_FLOATS * 4 + 15) & ~15);  // producer: range bounds
   static constexpr int BAR_OFF = SPLIT_OFF + 8 * (kSplitMaxCtas + 1);
-  static constexpr int NBARS = 2 + 4 * kKST + 2 * kMST + 8 + 3;
+  static constexpr int NBARS = 2 + 4 * kKST + 2 * kMST + 8 + 3 + 3;
   static constexpr int MISC_OFF = BAR_OFF + 8 * NBARS;
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + alignment slack
   // tensor memory columns
@@ -216,6 +216,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto pv_done = [&](int i) { return x0 + 48 + 8 * i; };
   const uint32_t xbar = x0 + 64;        // softmax-warp exchange (one arrival per softmax warp)
   const uint32_t mma_drain = x0 + 72;   // every MMA of an issuer complete (x0 + 72: scores, + 80: output)
+  // a head's merge: the other parts' (m, l) rows (+0) and their O^T halves, two parts in flight
+  auto merge_bar = [&](int i) { return x0 + 88 + 8 * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
@@ -242,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(xbar, C::NSM);
     mbar_init(mma_drain, 1);
     mbar_init(mma_drain + 8, 1);
+    for (int i = 0; i < 3; ++i) mbar_init(merge_bar(i), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -825,8 +828,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           p.ws_ml[((int64_t)b * 2 + 1) * kH + sid] = lsum;
         }
         if (had) {
-          float* w0 = p.ws_o + ((int64_t)b * kD + tr) * kH + hb;
-          float* w1 = p.ws_o + ((int64_t)b * kD + 128 + tr) * kH + hb;
+          // rows dv = tr and 128 + tr of O^T; the 16-byte granule of heads 4q .. 4q + 3 sits at
+          // position q ^ (tr & 15) of its 256-byte row, so that the merge reads the rows from
+          // shared memory without bank conflicts
+          float* w0 = p.ws_o + ((int64_t)b * kD + tr) * kH;
+          float* w1 = p.ws_o + ((int64_t)b * kD + 128 + tr) * kH;
 #pragma unroll 1
           for (int ch = 0; ch < C::CH; ++ch) {
             uint32_t o0[16], o1[16];
@@ -835,8 +841,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_wait_ld();
 #pragma unroll
             for (int i = 0; i < 16; i += 4) {
-              *reinterpret_cast<float4*>(w0 + 16 * ch + i) = make_float4(u2f(o0[i]), u2f(o0[i + 1]), u2f(o0[i + 2]), u2f(o0[i + 3]));
-              *reinterpret_cast<float4*>(w1 + 16 * ch + i) = make_float4(u2f(o1[i]), u2f(o1[i + 1]), u2f(o1[i + 2]), u2f(o1[i + 3]));
+              const int pos = 4 * ((((hb + 16 * ch + i) >> 2) ^ tr) & 15);
+              *reinterpret_cast<float4*>(w0 + pos) = make_float4(u2f(o0[i]), u2f(o0[i + 1]), u2f(o0[i + 2]), u2f(o0[i + 3]));
+              *reinterpret_cast<float4*>(w1 + pos) = make_float4(u2f(o1[i]), u2f(o1[i + 1]), u2f(o1[i + 2]), u2f(o1[i + 3]));
             }
           }
         }
@@ -872,14 +879,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!okp) fail(DSA_DEVERR_TIMEOUT);
       // (the launch keeps nparts <= kMaxParts; more would overrun the weight table)
       const int np = (okp && nparts <= kMaxParts) ? nparts : 0;
+      // The parts' rows come into shared memory by bulk copies: their (m, l) rows (consecutive
+      // workspace slots b+1 .. b+np) into the Q buffer, and their O^T halves into two slot
+      // pairs of the K stages, two parts in flight. A head segment is its CTA's last, so none of
+      // these buffers is in use any more: every output product is complete, and no further Q
+      // load or row load follows.
+      auto slot = [&](int pair, int half) -> uint32_t { return sbase + C::KT_OFF + (2 * pair + half) * (128 * kH * 4); };
+      auto fetch_part = [&](int u) {  // one thread: fill u = part u % np + 1 into slot pair u & 1
+        const uint32_t mb = merge_bar(1 + (u & 1));
+        const float* src = p.ws_o + (int64_t)(b + 1 + u % np) * kD * kH;
+        mbar_arrive_expect_tx(mb, kD * kH * 4);
+        bulk_g2s(slot(u & 1, 0), src, 128 * kH * 4, mb);
+        bulk_g2s(slot(u & 1, 1), src + 128 * kH, 128 * kH * 4, mb);
+      };
+      if (np > 0 && sid == 0) {
+        // the flags were acquired by this warp; order the parts' data (read by the async proxy)
+        // after them, and the buffers' earlier uses before the copies
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(merge_bar(0), np * 2 * kH * 4);
+        bulk_g2s(sbase + C::Q_OFF, p.ws_ml + (int64_t)(b + 1) * 2 * kH, np * 2 * kH * 4, merge_bar(0));
+        fetch_part(0);
+        if (np >= 2) fetch_part(1);
+      }
       if (sid < kH) {
+        const float* pml = reinterpret_cast<const float*>(smem + C::Q_OFF);  // [np][2][64]
+        if (np > 0 && !mbar_wait(merge_bar(0), 0, kWaitNs)) fail(DSA_DEVERR_TIMEOUT);
         float M = mrow;
-        for (int k = 1; k <= np; ++k) M = fmaxf(M, p.ws_ml[((int64_t)(b + k) * 2 + 0) * kH + sid]);
+        for (int k = 1; k <= np; ++k) M = fmaxf(M, pml[(k - 1) * 2 * kH + sid]);
         const float w_own = lsum > 0.0f ? exp2f(mrow - M) : 0.0f;
         float L = w_own * lsum;
         for (int k = 1; k <= np; ++k) {
-          const float mk = p.ws_ml[((int64_t)(b + k) * 2 + 0) * kH + sid];
-          const float lk = p.ws_ml[((int64_t)(b + k) * 2 + 1) * kH + sid];
+          const float mk = pml[((k - 1) * 2 + 0) * kH + sid];
+          const float lk = pml[((k - 1) * 2 + 1) * kH + sid];
           const float wk = lk > 0.0f ? exp2f(mk - M) : 0.0f;
           red_wk[(k - 1) * kH + sid] = wk;
           L += wk * lk;
@@ -890,11 +922,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.lse) p.lse[t * kH + sid] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
       }
       if (xsync(false) < 0) break;
-      // combine and stage the bf16 block [64 heads][256 columns] in the (idle) P buffers
+      // combine: this CTA's O (TMEM) and the parts in order, then stage the bf16 block
+      // [64 heads][256 columns] in the (idle) P buffers
       uint16_t* stage = reinterpret_cast<uint16_t*>(smem + C::P_OFF);
+      // One 16-head chunk at a time (32 accumulators): the parts stream through the two slot
+      // pairs in order, and with more than two parts the second chunk fetches them again.
+      bool okm = true;
+      int uses = 0;  // slot-pair fills consumed so far (fill u is part (u % np) + 1 in pair u & 1)
 #pragma unroll 1
-      for (int ch = 0; ch < C::CH; ++ch) {
+      for (int ch = 0; ch < C::CH && okm; ++ch) {
         const int h0 = hb + 16 * ch;
+        if (np <= 2) uses = 0;  // both parts stay in their slot pairs for the second chunk
         float acc0[16], acc1[16];
         const float* wo = red_alpha + h0;
         if (had) {
@@ -911,14 +949,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) acc0[i] = acc1[i] = 0.0f;
         }
-        for (int k = 1; k <= np; ++k) {
+        for (int k = 1; k <= np; ++k, ++uses) {
+          const int pr = uses & 1;
+          if (!wait_all(mbar_wait(merge_bar(1 + pr), (uses >> 1) & 1, kWaitNs))) {
+            okm = false;
+            break;
+          }
+          const uint8_t* r0 = smem + (slot(pr, 0) - sbase) + tr * 256;
+          const uint8_t* r1 = smem + (slot(pr, 1) - sbase) + tr * 256;
           const float* wk = red_wk + (k - 1) * kH + h0;
-          const float* s0 = p.ws_o + ((int64_t)(b + k) * kD + tr) * kH + h0;
-          const float* s1 = p.ws_o + ((int64_t)(b + k) * kD + 128 + tr) * kH + h0;
 #pragma unroll
           for (int i = 0; i < 16; i += 4) {
-            const float4 x = *reinterpret_cast<const float4*>(s0 + i);
-            const float4 y = *reinterpret_cast<const float4*>(s1 + i);
+            const int pos = 16 * ((((h0 + i) >> 2) ^ tr) & 15);
+            const float4 x = *reinterpret_cast<const float4*>(r0 + pos);
+            const float4 y = *reinterpret_cast<const float4*>(r1 + pos);
             acc0[i] += wk[i] * x.x;
             acc0[i + 1] += wk[i + 1] * x.y;
             acc0[i + 2] += wk[i + 2] * x.z;
@@ -928,13 +972,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             acc1[i + 2] += wk[i + 2] * y.z;
             acc1[i + 3] += wk[i + 3] * y.w;
           }
+          // the fill two ahead: the next part of this chunk's pass, or of the second chunk's
+          const int ahead = uses + 2, total = np > 2 ? C::CH * np : np;
+          if (ahead < total) {
+            // every warp has read this slot pair: refill it
+            if (xsync(false) < 0) {
+              okm = false;
+              break;
+            }
+            if (sid == 0) {
+              fence_proxy_async_smem();
+              fetch_part(ahead);
+            }
+          }
         }
+        if (!okm) break;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           stage[(h0 + i) * kD + tr] = __bfloat16_as_ushort(__float2bfloat16_rn(acc0[i]));
           stage[(h0 + i) * kD + 128 + tr] = __bfloat16_as_ushort(__float2bfloat16_rn(acc1[i]));
         }
       }
+      if (!okm) break;
       if (xsync(false) < 0) break;
       // every softmax warp has read the parts: clear their publish flags, so that the workspace
       // holds no set flag after the call (a later call that carries the same tag, such as a
@@ -1290,9 +1349,10 @@ dsa_status_t plan_unit_split(const dsa_attn_args_t* a, const DeviceInfo& dev, co
   UnitSplit r;
   r.NT = (a->topk + kBN - 1) / kBN;
   r.U = a->T * (int64_t)r.NT;
-  // one persistent CTA per SM, with at least 4 units per CTA (small batches split each token
-  // into few parts), and few enough CTAs that a token spans at most kMaxParts + 1 of them
-  int64_t G = (r.U + 3) / 4;
+  // one persistent CTA per SM, with at least 2 units per CTA (a small batch spreads over many
+  // CTAs: the parts of a split token are merged from bulk copies in shared memory), and few
+  // enough CTAs that a token spans at most kMaxParts + 1 of them
+  int64_t G = (r.U + 1) / 2;
   if (G > dev.sm_count) G = dev.sm_count;
   while (G > 1) {
     const int64_t upc = r.U / G;  // fewest units any CTA holds
