@@ -8,6 +8,8 @@
 // bf16. The cache holds bf16 rows or the packed scaled-FP8 rows of the Contract table (256
 // e4m3 codes, then one fp32 scale per 128-column tile).
 //
+// This file holds the bf16-cache kernel; packed FP8 rows run in dsa_attn_f8.cu.
+//
 // Kernel design (GB300-first, not the pages' TileLang/HIP kernels):
 //  * Transposed products. Scores: S^T[key, head] = K Q^T with M = 128 gathered keys, N = 64
 //    heads, K-dim 256; output: O^T[dv, head] += V^T P^T in two M = 128 halves of d_v, V^T read
@@ -15,25 +17,19 @@
 //    key). tcgen05 kind::f16, bf16 operands, fp32 accumulators in tensor memory with lane =
 //    key (scores) or lane = output column (O). M = 128 keeps the tensor core at full width,
 //    where heads as M (M = 64) would use half of it.
-//  * Packed FP8 rows are widened to bf16 exactly and without their scales. The two tile scales
-//    belong to one key, i.e. one accumulator lane, so they are applied in fp32 where that lane
-//    is read: the score is sc0 * S_0 + sc1 * S_1 (S_t accumulates the columns of tile t), and
-//    the probabilities that multiply tile t of V are p * sc_t (two P buffers, one per tile).
-//  * Softmax per key: one thread per TMEM lane holds its key's 64 scores. The running max of
-//    each head (exp2 domain) lives in shared memory and is raised only when a tile exceeds it by
-//    more than 2^8 (a CTA-wide vote of the four softmax warps); the first tile of a segment
-//    takes exact per-head maxima with warp max-reductions. Partial row sums per lane accumulate
-//    in TMEM and are reduced across lanes once per token.
+//  * Softmax per key: one thread per TMEM lane holds its key's scores of 32 heads (two warps
+//    per TMEM lane quarter). The running max of each head (exp2 domain) lives in shared memory
+//    and is raised only when a tile exceeds it by more than 2^8 (a vote of the eight softmax
+//    warps); the first tile of a segment takes exact per-head maxima with warp max-reductions.
+//    Partial row sums per lane accumulate in TMEM and are reduced across lanes once per token.
 //  * Persistent cooperative launch, one CTA per SM; (token, 128-position tile) units split into
 //    contiguous ranges per CTA; a token cut by a range boundary is merged in-kernel by the CTA
-//    holding its first tiles (fixed order, no atomics on data).
+//    holding its first tiles (fixed order, no atomics on data), from the other parts' partial
+//    results brought into shared memory by bulk copies.
 //  * Warp roles: 0 producer (index read, -1 compaction into dense 128-key tiles, page
-//    translation, Q loads by TMA), 1 score-MMA issuer, 2 output-MMA issuer, then softmax and
-//    epilogue warps and row loaders: for packed rows 4-7 softmax, 8-15 loaders (copies of
-//    packed half rows into a ring, widened into the 128-byte-swizzled K tile); for bf16 rows,
-//    whose loaders only issue cp.async copies straight into the tile, 4-11 softmax (two warps
-//    per TMEM lane quarter, 32 heads each) and 3, 12-15 loaders. Packed rows are not prefetched
-//    into L2: the extra whole-line traffic cost more than it saved.
+//    translation, Q loads by TMA), 1 score-MMA issuer, 2 output-MMA issuer, 4-11 softmax and
+//    epilogue, 3 and 12-15 row loaders (16-byte cp.async copies straight into the K tile,
+//    loaded and released in two column halves).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -56,7 +52,6 @@ constexpr int kMST = 8;         // meta ring depth
 constexpr int kWarps = 16;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kMaxParts = 16;     // most parts of one split token (the launch guarantees it)
-constexpr int kRing = 8;          // ring of a packed-row loader warp: 2 units of 8 half rows (2 KB)
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kSplitMaxCtas = 192;  // most CTAs of a work-balanced split (its bounds live in shared memory)
 constexpr int kSplitSlices = 32;    // unit slices per CTA counted by the split pre-pass
@@ -65,45 +60,30 @@ constexpr int kSplitSlices = 32;    // unit slices per CTA counted by the split 
 // hold one-tile and sixteen-tile tokens put that at about 5.5 full tiles.
 constexpr int kSegmentWeight = 704;
 
-template <int KIND>
 struct Cfg {
-  static constexpr bool FP8 = KIND == DSA_CACHE_FP8_SCALED;
-  static constexpr int RB = FP8 ? 264 : 512;  // cache row bytes
-  // Warp roles: 0 producer, 1 score-MMA issuer, 2 output-MMA issuer, 4 .. 3 + NSM softmax (warp
-  // w takes TMEM lane quarter w % 4; with eight, the two warps of a quarter split the heads),
-  // then the row loaders. Packed rows: four softmax warps and eight loaders, warps 8-15, two on
-  // each SM sub-partition (warp w runs on sub-partition w % 4), which their dequantisation
-  // needs; warp 3 stays idle, since a ninth loader beside softmax warp 7 slows the warp that
-  // every tile's vote waits for. bf16 rows are plain copies: eight softmax warps and five
-  // loaders, warps 3 and 12-15.
-  static constexpr int NSM = FP8 ? 4 : 8;
-  static constexpr int NLD = FP8 ? 8 : 5;
+  static constexpr int RB = 512;  // cache row bytes (256 bf16)
+  // Warp roles: 0 producer, 1 score-MMA issuer, 2 output-MMA issuer, 4-11 softmax (warp w takes
+  // TMEM lane quarter w % 4; the two warps of a quarter split the heads), 3 and 12-15 loaders.
+  static constexpr int NSM = 8;
+  static constexpr int NLD = 5;
   static constexpr int HW = kH * 4 / NSM;  // heads per softmax warp
   static constexpr int CH = HW / 16;       // 16-head chunks per softmax warp
   static constexpr int NR = (kBN + NLD - 1) / NLD;  // most rows of a tile per loader warp
   // loader index of a warp, -1 for other warps
-  static __device__ __forceinline__ int loader_index(int warp) {
-    if constexpr (FP8) return warp >= 8 ? warp - 8 : -1;
-    else return warp == 3 ? 0 : (warp >= 12 ? warp - 11 : -1);
-  }
-  static constexpr int NSUB = FP8 ? 2 : 1;    // score accumulators per tile (one per scale tile)
-  static constexpr int PBUF = FP8 ? 1 : 2;    // P buffers
-  static constexpr int P_BYTES = NSUB * kBN * 128;
+  static __device__ __forceinline__ int loader_index(int warp) { return warp == 3 ? 0 : (warp >= 12 ? warp - 11 : -1); }
+  static constexpr int PBUF = 2;  // P buffers
+  static constexpr int P_BYTES = kBN * 128;
   // shared memory carve-up (offsets from a 1024-aligned base)
   static constexpr int Q_OFF = 0;
   static constexpr int Q_BYTES = kH * kD * 2;
   static constexpr int KT_OFF = Q_OFF + Q_BYTES;
   static constexpr int KT_BYTES = kBN * kD * 2;
   static constexpr int P_OFF = KT_OFF + kKST * KT_BYTES;
-  static constexpr int SC_OFF = P_OFF + PBUF * P_BYTES;
-  static constexpr int SC_BYTES = FP8 ? kBN * 8 : 0;  // per stage: (scale0, scale1) per row
-  static constexpr int META_OFF = SC_OFF + kKST * SC_BYTES;
+  static constexpr int META_OFF = P_OFF + PBUF * P_BYTES;
   static constexpr int META_BYTES = 32 + 4 * kBN;
   static constexpr int CMP_OFF = META_OFF + kMST * META_BYTES;  // producer: one step's valid slots
-  static constexpr int RING_OFF = CMP_OFF + 4 * 256;                // packed-row loaders: code rings
-  static constexpr int RING_BYTES = FP8 ? NLD * kRing * 256 : 0;
-  static constexpr int RED_OFF = RING_OFF + RING_BYTES;
-  // m[64], alpha[64], lsum[64], spare[64], part[4][64], wk[kMaxParts][64], votes[2][8]
+  static constexpr int RED_OFF = CMP_OFF + 4 * 256;
+  // m[64], alpha[64], spare[128], part[4][64], wk[kMaxParts][64], votes[2][8]
   static constexpr int RED_FLOATS = 8 * kH + kMaxParts * kH + 2 * NSM;
   static constexpr int SPLIT_OFF = RED_OFF + ((RED_FLOATS * 4 + 15) & ~15);  // producer: range bounds
   static constexpr int BAR_OFF = SPLIT_OFF + 8 * (kSplitMaxCtas + 1);
@@ -111,13 +91,14 @@ struct Cfg {
   static constexpr int MISC_OFF = BAR_OFF + 8 * NBARS;
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + alignment slack
   // tensor memory columns
-  static constexpr int S_COLS = 64 * NSUB;  // per S buffer (two buffers)
-  static constexpr int O_COL = 2 * S_COLS;  // O^T halves: dv 0-127 at O_COL, dv 128-255 at O_COL + 64
+  static constexpr int S_COLS = 64;          // per S buffer (two buffers)
+  static constexpr int O_COL = 2 * S_COLS;   // O^T halves: dv 0-127 at O_COL, dv 128-255 at O_COL + 64
   static constexpr int L_COL = O_COL + 128;  // per-lane partial row sums, two buffers of 64 columns
   static constexpr int TMEM_COLS = 512;
   static_assert(L_COL + 128 <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(KT_OFF % 1024 == 0 && P_OFF % 1024 == 0 && KT_BYTES % 1024 == 0, "operand alignment");
+  static_assert(CH == 2, "two 16-head chunks per softmax warp");
 };
 
 // meta ring entry types and segment kinds
@@ -193,10 +174,9 @@ static __device__ __noinline__ int softmax_exchange(uint32_t xbar, int* votes, u
   return r ? 1 : 0;
 }
 
-template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_k128_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmap_q) {
-  using C = Cfg<KIND>;
+  using C = Cfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -226,8 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(q_empty, 1);
     for (int s = 0; s < kKST; ++s) {
       for (int h = 0; h < 2; ++h) {
-        // bf16 rows: one cp.async arrive per loader thread; packed rows: one per loader warp
-        mbar_init(k_full(s, h), C::FP8 ? C::NLD : 32 * C::NLD);
+        mbar_init(k_full(s, h), 32 * C::NLD);  // one cp.async arrive per loader thread
         mbar_init(k_empty(s, h), 1);
       }
     }
@@ -512,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int ks = g % kKST;
         if (warp == 1) {
-          // ---- scores S^T = K Q^T for tile g (two 64-column sub-accumulators for packed rows)
+          // ---- scores S^T = K Q^T for tile g
           if (first) {
             if (!wait(q_full, qc & 1)) break;
             ++qc;
@@ -520,25 +499,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (g >= 2 && !wait(s_empty(g & 1), ((g >> 1) & 1) ^ 1)) break;
           const uint32_t k_lo = (uint32_t)sw128_desc(sbase + C::KT_OFF + ks * C::KT_BYTES, 16, 1024);
           const uint32_t d0 = tmem + (g & 1) * C::S_COLS;
-          // 16-column step kk: chunk kk/4 of 64 columns, 32 bytes per step inside the chunk;
-          // packed rows accumulate columns 0-127 and 128-255 separately (one scale each)
+          // 16-column step kk: chunk kk/4 of 64 columns, 32 bytes per step inside the chunk
           auto step = [&](int kk) {
             const uint32_t ka = (uint32_t)((kk >> 2) * ((kBN * 128) >> 4) + (kk & 3) * 2);
             const uint32_t qa = (uint32_t)((kk >> 2) * ((kH * 128) >> 4) + (kk & 3) * 2);
-            const uint32_t d = C::FP8 ? d0 + 64 * (kk >> 3) : d0;
-            if ((C::FP8 ? (kk & 7) : kk) == 0) mma_bf16_lohi<0>(d, k_lo + ka, k_hi, q_lo + qa, q_hi, idS);
-            else mma_bf16_lohi<1>(d, k_lo + ka, k_hi, q_lo + qa, q_hi, idS);
+            if (kk == 0) mma_bf16_lohi<0>(d0, k_lo + ka, k_hi, q_lo + qa, q_hi, idS);
+            else mma_bf16_lohi<1>(d0, k_lo + ka, k_hi, q_lo + qa, q_hi, idS);
           };
           // the first column half's products start while the loaders write the second half
           if (!wait(k_full(ks, 0), (g / kKST) & 1)) break;
-          // bf16 rows arrive by cp.async (generic proxy): order them before the tensor core
-          // reads (the packed-row loaders fence on their side before arriving)
-          if constexpr (!C::FP8) fence_proxy_async_smem();
+          // rows arrive by cp.async (generic proxy): order them before the tensor core reads
+          fence_proxy_async_smem();
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kD / 32; ++kk) step(kk);
           if (!wait(k_full(ks, 1), (g / kKST) & 1)) break;
-          if constexpr (!C::FP8) fence_proxy_async_smem();
+          fence_proxy_async_smem();
           tc_fence_after();
 #pragma unroll
           for (int kk = kD / 32; kk < kD / 16; ++kk) step(kk);
@@ -551,12 +527,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t v_lo = (uint32_t)sw128_desc(sbase + C::KT_OFF + ks * C::KT_BYTES, kBN * 128, 1024);
           const uint32_t p_lo = (uint32_t)sw128_desc(sbase + C::P_OFF + (g % C::PBUF) * C::P_BYTES, kBN * 128, 1024);
           // output columns 128h .. 128h + 127 (V^T two 64-column groups further); 16 keys per
-          // step (16 rows of 128 bytes); packed rows take p * scale of tile h
+          // step (16 rows of 128 bytes)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const uint32_t d = tmem + C::O_COL + 64 * h;
             const uint32_t va = v_lo + h * ((2 * kBN * 128) >> 4);
-            const uint32_t pa = p_lo + (C::FP8 ? h * ((kBN * 128) >> 4) : 0);
+            const uint32_t pa = p_lo;
             // the first step of a segment's first tile overwrites the accumulator
             mma_bf16(d, ((uint64_t)mn_hi << 32) | va, ((uint64_t)mn_hi << 32) | pa, idPV, first ? 0u : 1u);
 #pragma unroll
@@ -575,9 +551,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp >= 4 && warp < 4 + C::NSM) {  // (softmax)
-    // ================================== softmax + epilogue (4 or 8 warps, C::NSM) ====
-    // Thread = key of the tile = TMEM lane (quarter warp % 4); with eight warps the two warps
-    // of a quarter take heads 0-31 and 32-63. Per tile one pass computes, with the running max m_h of each head,
+    // ============================================= softmax + epilogue (8 warps) ====
+    // Thread = key of the tile = TMEM lane (quarter warp % 4); the two warps of a quarter take
+    // heads 0-31 and 32-63. Per tile one pass computes, with the running max m_h of each head,
     // x = c * score - m_h, p = 2^x, the per-lane partial row sums (TMEM, two buffers: the pass
     // reads one and writes the other) and the probability rows of P. A vote of the warps
     // then checks that no x exceeded 8; if one did (rare after a segment's first tile), the
@@ -627,31 +603,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(m_empty(st));
         ++mc;
-        const int ks = g % kKST;
         bool ok = mbar_wait(s_full(g & 1), (g >> 1) & 1, kWaitNs);
-        // the tile scales come from the loaders: acquire their stage barrier directly
-        if constexpr (C::FP8) ok = ok && mbar_wait(k_full(ks, 1), (g / kKST) & 1, kWaitNs);
         // the P buffer must be free: the PV product that read it last is complete
         ok = ok && pv_wait((int64_t)g - C::PBUF);
         if (!wait_all(ok)) break;
         tc_fence_after();
         const bool valid = tr < n_valid;
-        float sc0 = 1.0f, sc1 = 0.0f;
-        if constexpr (C::FP8) {
-          const float2 sc = *reinterpret_cast<const float2*>(smem + C::SC_OFF + ks * C::SC_BYTES + tr * 8);
-          sc0 = sc.x;
-          sc1 = sc.y;
-        }
-        const float c0 = p.c_log2 * sc0, c1 = p.c_log2 * sc1;
+        const float c0 = p.c_log2;
         const uint32_t sa = tl + (g & 1) * C::S_COLS + hb;
         const uint32_t lcur = tl + C::L_COL + 64 * lb + hb, lnxt = tl + C::L_COL + 64 * (lb ^ 1) + hb;
         uint8_t* prow = smem + C::P_OFF + (g % C::PBUF) * C::P_BYTES + tr * 128;
         const int sw = tr & 7;
         // score of head i of a chunk, exp2 domain, before subtracting the running max
-        auto score = [&](const uint32_t (&a)[16], const uint32_t (&bb)[16], int i) -> float {
-          if constexpr (C::FP8) return fmaf(u2f(a[i]), c0, u2f(bb[i]) * c1);
-          else return u2f(a[i]) * c0;
-        };
+        auto score = [&](const uint32_t (&a)[16], int i) -> float { return u2f(a[i]) * c0; };
         bool exact = first != 0, bad = false;
         for (;;) {
           bool resc = false;
@@ -660,13 +624,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // across the four lane quarters
 #pragma unroll 1
             for (int ch = 0; ch < C::CH; ++ch) {
-              uint32_t a[16], bb[16];
+              uint32_t a[16];
               tmem_ld32_x16(sa + 16 * ch, a);
-              if constexpr (C::FP8) tmem_ld32_x16(sa + 64 + 16 * ch, bb);
               tc_wait_ld();
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
-                const int mx = redux_max_s32(f2ord(valid ? score(a, bb, i) : -INFINITY));
+                const int mx = redux_max_s32(f2ord(valid ? score(a, i) : -INFINITY));
                 if (lane == ((16 * ch + i) & 31)) red_part[qd * 64 + hb + 16 * ch + i] = ord2f(mx);
               }
             }
@@ -711,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           // the pass: p = 2^(c * score - m) (one FFMA and one MUFU ex2 per score), partial row
           // sums into the other TMEM buffer (a rescale has already scaled the buffer it reads),
-          // and P (packed rows: p * scale of each tile) as bf16 into this key's 128-byte row
+          // and P as bf16 into this key's 128-byte row
           float xm = -INFINITY;
 #pragma unroll 1
           for (int ch = 0; ch < C::CH; ++ch) {
@@ -719,15 +682,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 16; i += 4)
               *reinterpret_cast<float4*>(mv + i) = *reinterpret_cast<const float4*>(red_m + hb + 16 * ch + i);
-            uint32_t a[16], bb[16], l[16];
+            uint32_t a[16], l[16];
             tmem_ld32_x16(sa + 16 * ch, a);
-            if constexpr (C::FP8) tmem_ld32_x16(sa + 64 + 16 * ch, bb);
             if (!first) tmem_ld32_x16(lcur + 16 * ch, l);
             tc_wait_ld();
             float pr[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const float x = score(a, bb, i) - mv[i];
+              const float x = score(a, i) - mv[i];
               xm = fmaxf(xm, valid ? x : -INFINITY);
               pr[i] = valid ? ex2_approx(x) : 0.0f;
               float lv = pr[i];
@@ -738,15 +700,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int g0 = (hb >> 3) + 2 * ch;  // 16-byte granules of this chunk's 16 heads
             uint32_t w[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) w[i] = f32x2_to_bf16x2(pr[2 * i] * sc0, pr[2 * i + 1] * sc0);
+            for (int i = 0; i < 8; ++i) w[i] = f32x2_to_bf16x2(pr[2 * i], pr[2 * i + 1]);
             *reinterpret_cast<uint4*>(prow + ((g0 ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
             *reinterpret_cast<uint4*>(prow + (((g0 + 1) ^ sw) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
-            if constexpr (C::FP8) {
-#pragma unroll
-              for (int i = 0; i < 8; ++i) w[i] = f32x2_to_bf16x2(pr[2 * i] * sc1, pr[2 * i + 1] * sc1);
-              *reinterpret_cast<uint4*>(prow + kBN * 128 + ((g0 ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-              *reinterpret_cast<uint4*>(prow + kBN * 128 + (((g0 + 1) ^ sw) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
-            }
           }
           if (exact) break;
           const int r = xsync(xm > 8.0f);
@@ -1012,7 +968,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
     }
   } else if (C::loader_index(warp) >= 0) {
-    // ================================================= row loaders (C::NLD warps) ====
+    // ================================================= row loaders (5 warps) ====
     // Warp dw fills rows dw + C::NLD * k (k < nk) of each K tile in the 128-byte-swizzled K-major
     // layout (row r, 16-byte granule q of 64-column chunk c at c*128*128 + r*128 + ((q ^ (r&7)) << 4)).
     // A tile is written in two column halves, columns 0-127 (chunks 0-1) and 128-255 (chunks
@@ -1024,8 +980,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Rows past n_valid are zero (their keys are masked: a zero row keeps 0 * V finite).
     const int dw = C::loader_index(warp);
     const int nk = (kBN - dw + C::NLD - 1) / C::NLD;  // rows of this warp per tile: dw + C::NLD * k, k < nk
-    // lane t holds the slot of row dw + NLD * t; packed rows are taken as eight row pairs
-    static_assert(C::NR <= (C::FP8 ? 16 : 32), "a warp's rows of a tile fit its lanes");
+    // lane t holds the slot of row dw + NLD * t
+    static_assert(C::NR <= 32, "a warp's rows of a tile fit its lanes");
     const int hl = lane >> 4, il = lane & 15;
     uint32_t mc = 0, g = 0;
     auto next_tile = [&](bool block, int& st_out) -> int {
@@ -1046,35 +1002,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return 0;
     };
-    // tile in meta slot st: row count, lane t's slot of row dw + C::NLD * t (-1 past the valid
-    // rows) and, for packed rows, its two scales. Everything the loader needs of the entry is
-    // then in registers: the caller releases the meta stage right away, and a copy takes the
-    // slot of row k from lane k by a shuffle.
-    auto take = [&](int st, int& n, int& slr, float2& scale) {
+    // tile in meta slot st: row count and lane t's slot of row dw + C::NLD * t (-1 past the
+    // valid rows). Everything the loader needs of the entry is then in registers: the caller
+    // releases the meta stage right away, and a copy takes the slot of row k from lane k by a
+    // shuffle.
+    auto take = [&](int st, int& n, int& slr) {
       const MetaHdr* mh = reinterpret_cast<const MetaHdr*>(smem + C::META_OFF + st * C::META_BYTES);
       n = mh->n_valid;
       const int* slots = reinterpret_cast<const int*>(reinterpret_cast<const uint8_t*>(mh) + 32);
       const int rt = dw + C::NLD * lane;
       slr = -1;
-      scale = make_float2(0.0f, 0.0f);
-      if (lane < nk && rt < n) {
-        slr = slots[rt];
-        if constexpr (C::FP8) scale = __ldg(reinterpret_cast<const float2*>(p.cache + (int64_t)slr * C::RB + kD));
-      }
+      if (lane < nk && rt < n) slr = slots[rt];
     };
     auto release = [&]() {
       __syncwarp();
       if (lane == 0) mbar_arrive(m_empty(mc % kMST));
       ++mc;
     };
-    if constexpr (!C::FP8) {
-      // bf16 rows: 16-byte cp.async straight into the tile, one row pair per instruction; each
-      // thread's copies of a half signal that half's full barrier when they land
+    {
+      // 16-byte cp.async straight into the tile, one row pair per instruction; each thread's
+      // copies of a half signal that half's full barrier when they land
       int st = 0, n = 0, slr = -1;
-      float2 unused;
       bool bad = false;
       while (!bad && next_tile(true, st) == 1) {
-        take(st, n, slr, unused);
+        take(st, n, slr);
         release();
         const int ks = g % kKST;
         uint8_t* kt = smem + C::KT_OFF + ks * C::KT_BYTES;
@@ -1090,7 +1041,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int sl = __shfl_sync(0xffffffffu, slr, k);
             if (k < nk) {
               const int r = dw + C::NLD * k;
-              const uint8_t* src = p.cache + (sl >= 0 ? (int64_t)sl : 0) * (2 * kD) + 16 * G;
+              const uint8_t* src = p.cache + (sl >= 0 ? (int64_t)sl : 0) * C::RB + 16 * G;
               const uint32_t dst = smem_u32(kt + (G >> 3) * (kBN * 128) + r * 128 + (((G & 7) ^ (r & 7)) << 4));
               asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(sl >= 0 ? 16 : 0)
                            : "memory");
@@ -1099,110 +1050,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(k_full(ks, h)) : "memory");
         }
         ++g;
-      }
-    } else {
-      // Packed rows, one column half at a time. A unit is four row pairs of one half (8 x 128
-      // codes = 1 KB); a lane copies 8 codes of its row by an 8-byte cp.async (a packed row is
-      // 8-byte aligned, so the copy carries exactly the codes it needs) into a two-unit ring
-      // per warp, one commit group per unit. A tile is four units: half 0 pairs 0-3 and 4-7,
-      // then half 1. The widening loop waits for the older unit, widens each lane's 8 codes per
-      // pair into one output granule, and refills the unit's ring slot with the unit two ahead,
-      // of this tile or (once its meta entry is published) of the next one.
-      const uint32_t ring_s = smem_u32(smem + C::RING_OFF + dw * 2048) + hl * 128 + 8 * il;
-      const uint8_t* ring_g = smem + C::RING_OFF + dw * 2048 + hl * 128 + 8 * il;
-      auto copy_unit = [&](int slr, int u) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int k = 2 * (4 * (u & 1) + q) + hl;
-          const int sl = __shfl_sync(0xffffffffu, slr, k);
-          if (sl >= 0) {
-            const uint8_t* src = p.cache + (int64_t)sl * C::RB + 128 * (u >> 1) + 8 * il;
-            asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(ring_s + (u & 1) * 1024 + q * 256), "l"(src)
-                         : "memory");
-          }
-        }
-        asm volatile("cp.async.commit_group;" ::: "memory");
-      };
-      int st_c = 0, n_c = 0, st_n = -1, n_n = 0, sl_c = -1, sl_n = -1;
-      float2 sc_c = make_float2(0.0f, 0.0f), sc_n = make_float2(0.0f, 0.0f);
-      bool have_n = false;
-      int look = -1;  // lookahead: 1 next tile taken, 0 end of stream, -1 not published yet
-      auto look_ahead = [&]() {
-        if (have_n || look == 0) return;
-        int stx = -1;
-        look = next_tile(false, stx);
-        if (look == 1) {
-          st_n = stx;
-          take(st_n, n_n, sl_n, sc_n);
-          release();
-          have_n = true;
-        }
-      };
-      int r = next_tile(true, st_c);
-      if (r == 1) {
-        take(st_c, n_c, sl_c, sc_c);
-        release();
-        copy_unit(sl_c, 0);
-        copy_unit(sl_c, 1);
-      }
-      while (r == 1) {
-        look_ahead();  // the next tile's entry, while this one's stage may still be busy
-        const int ks = g % kKST;
-        uint8_t* kt = smem + C::KT_OFF + ks * C::KT_BYTES;
-        const bool full = n_c == kBN;  // every row valid: no zero rows to write
-        bool bad = false;
-#pragma unroll 1
-        for (int u = 0; u < 4; ++u) {
-          const int h = u >> 1;
-          if ((u & 1) == 0 && g >= (uint32_t)kKST && !wait(k_empty(ks, h), ((g / kKST) & 1) ^ 1)) {
-            bad = true;
-            break;
-          }
-          asm volatile("cp.async.wait_group 1;" ::: "memory");
-          uint2 w[4];  // all four ring reads first: one shared-memory round trip
-#pragma unroll
-          for (int q = 0; q < 4; ++q) w[q] = *reinterpret_cast<const uint2*>(ring_g + (u & 1) * 1024 + q * 256);
-          const int G = 16 * h + il;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int k = 2 * (4 * (u & 1) + q) + hl, rr = dw + C::NLD * k;
-            uint4 o = make_uint4(e4m3x2_to_bf16x2_exact<0x9180u>(w[q].x), e4m3x2_to_bf16x2_exact<0xB3A2u>(w[q].x),
-                                 e4m3x2_to_bf16x2_exact<0x9180u>(w[q].y), e4m3x2_to_bf16x2_exact<0xB3A2u>(w[q].y));
-            if (!full && rr >= n_c) o = make_uint4(0u, 0u, 0u, 0u);
-            if (k < nk) *reinterpret_cast<uint4*>(kt + (G >> 3) * (kBN * 128) + rr * 128 + (((G & 7) ^ (rr & 7)) << 4)) = o;
-          }
-          __syncwarp();  // every lane has read the unit's ring slot before it is refilled
-          if (u < 2) {
-            copy_unit(sl_c, u + 2);
-          } else {
-            if (u == 2) look_ahead();
-            copy_unit(have_n ? sl_n : -1, u - 2);
-          }
-          if (u & 1) {  // column half h of the tile is written
-            if (h == 1 && lane < nk)
-              *reinterpret_cast<float2*>(smem + C::SC_OFF + ks * C::SC_BYTES + (dw + C::NLD * lane) * 8) = sc_c;
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(k_full(ks, h));
-          }
-        }
-        if (bad) break;
-        ++g;
-        if (have_n) {
-          st_c = st_n;
-          n_c = n_n;
-          sl_c = sl_n;
-          sc_c = sc_n;
-          have_n = false;
-          continue;
-        }
-        if (look == 0) break;  // the lookahead already consumed the end of the stream
-        r = next_tile(true, st_c);
-        if (r != 1) break;
-        take(st_c, n_c, sl_c, sc_c);
-        release();
-        copy_unit(sl_c, 0);
-        copy_unit(sl_c, 1);
       }
     }
     // drain this thread's outstanding cp.async copies before the CTA can finish
@@ -1384,9 +1231,8 @@ dsa_status_t plan_unit_split(const dsa_attn_args_t* a, const DeviceInfo& dev, co
 
 namespace k128 {
 
-template <int KIND>
 static dsa_status_t launch(const dsa_attn_args_t* a, const DeviceInfo& dev, cudaStream_t stream) {
-  using C = Cfg<KIND>;
+  using C = Cfg;
   CUtensorMap tq;
   dsa_status_t st = encode_q_tensor_map(a, kD, &tq);
   if (st != DSA_OK) return st;
@@ -1442,19 +1288,19 @@ static dsa_status_t launch(const dsa_attn_args_t* a, const DeviceInfo& dev, cuda
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_k128_kernel<KIND>, p, tq);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_k128_kernel, p, tq);
   return e == cudaSuccess ? DSA_OK : cuda_fail(e);
 }
 
 }  // namespace k128
 
 cudaError_t k128_set_attributes() {
-  return cudaFuncSetAttribute(k128::attn_k128_kernel<DSA_CACHE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              k128::Cfg<DSA_CACHE_BF16>::SMEM_BYTES);
+  return cudaFuncSetAttribute(k128::attn_k128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              k128::Cfg::SMEM_BYTES);
 }
 
 dsa_status_t launch_attn_k128(const dsa_attn_args_t* a, const DeviceInfo& dev, cudaStream_t stream) {
-  if (a->kind == DSA_CACHE_BF16) return k128::launch<DSA_CACHE_BF16>(a, dev, stream);
+  if (a->kind == DSA_CACHE_BF16) return k128::launch(a, dev, stream);
   return launch_attn_f8(a, dev, stream);
 }
 

@@ -311,20 +311,4 @@ __device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
   return r;
 }
 
-// Exact widening of two e4m3 codes to bf16 without a scale. `sel` picks the two source bytes of
-// `w` with the sign of each replicated into the byte above it (0x9180: bytes 0, 1; 0xB3A2:
-// bytes 2, 3). Shifting sign-extended 16-bit halves left by 4 and keeping bits 0x87F0 puts the
-// code's sign at bf16 bit 15 and its 4-bit exponent and 3-bit mantissa at bits 10..4, i.e. a
-// bf16 with the code's value times 2^-120 (e4m3 subnormals land on bf16 subnormals); the
-// multiply by 2^120 (bf16 0x7B80) is exact. Codes 0x7F / 0xFF (NaN in e4m3) are never written
-// by the packer and would read as +-480.
-template <uint32_t SEL>
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_exact(uint32_t w) {
-  uint32_t t, r;
-  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(t) : "r"(w), "n"(SEL));
-  t = (t << 4) & 0x87F087F0u;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(0x7B807B80u));
-  return r;
-}
-
 }  // namespace dsa
