@@ -999,12 +999,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_f8_kernel(const __grid_const
       auto slot = [&](int pair, int half) -> uint32_t {
         return sbase + (pair == 0 ? KT_OFF + half * KT_BYTES : (half == 0 ? KT_OFF + 2 * KT_BYTES : P_OFF + P_BYTES));
       };
-      auto fetch_part = [&](int u) {  // one thread: fill u = part u % np + 1 into slot pair u & 1
-        const uint32_t mb = merge_bar(1 + (u & 1));
-        const float* src = p.ws_o + (int64_t)(b + 1 + u % np) * kD * kH;
+      auto fetch_part = [&](int k) {  // one thread: part k (1-based) into slot pair (k - 1) & 1
+        const uint32_t mb = merge_bar(1 + ((k - 1) & 1));
+        const float* src = p.ws_o + (int64_t)(b + k) * kD * kH;
         mbar_arrive_expect_tx(mb, kD * kH * 4);
-        bulk_g2s(slot(u & 1, 0), src, 128 * kH * 4, mb);
-        bulk_g2s(slot(u & 1, 1), src + 128 * kH, 128 * kH * 4, mb);
+        bulk_g2s(slot((k - 1) & 1, 0), src, 128 * kH * 4, mb);
+        bulk_g2s(slot((k - 1) & 1, 1), src + 128 * kH, 128 * kH * 4, mb);
       };
       if (np > 0 && sid == 0) {
         // the flags were acquired by this warp; order the parts' data (read by the async proxy)
@@ -1013,8 +1013,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_f8_kernel(const __grid_const
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(merge_bar(0), np * 4 * kH * 4);
         bulk_g2s(sbase + Q_OFF, wsml + (int64_t)(b + 1) * 4 * kH, np * 4 * kH * 4, merge_bar(0));
-        fetch_part(0);
-        if (np >= 2) fetch_part(1);
+        fetch_part(1);
+        if (np >= 2) fetch_part(2);
       }
       if (sid < kH) {
         // sums relative to the largest m over the parts; each half's O of each part weighted
@@ -1044,72 +1044,59 @@ __global__ void __launch_bounds__(kThreads, 1) attn_f8_kernel(const __grid_const
       // combine: this CTA's O (TMEM) and the parts in order, then stage the bf16 block
       // [64 heads][256 columns] in P buffer 0 (idle: every output product is complete)
       uint16_t* stage = reinterpret_cast<uint16_t*>(smem + P_OFF);
-      // One 16-head chunk at a time (32 accumulators): the parts stream through the two slot
-      // pairs in order, and with more than two parts the second chunk fetches them again.
+      // The sum accumulates in this CTA's O columns of tensor memory (lane = d_v row): first its
+      // own O times its weights, then each part in order as it lands, one 16-head chunk at a
+      // time; the last step writes bf16 to the stage instead.
       bool okm = true;
-      int uses = 0;  // slot-pair fills consumed so far (fill u is part (u % np) + 1 in pair u & 1)
-#pragma unroll 1
-      for (int ch = 0; ch < 2 && okm; ++ch) {
-        const int h0 = hb + 16 * ch;
-        if (np <= 2) uses = 0;  // both parts stay in their slot pairs for the second chunk
-        float acc0[16], acc1[16];
-        if (had) {
-          uint32_t o0[16], o1[16];
-          tmem_ld32_x16(tl + O_COL + h0, o0);
-          tmem_ld32_x16(tl + O_COL + 64 + h0, o1);
-          tc_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            acc0[i] = red_al[h0 + i] * u2f(o0[i]);
-            acc1[i] = red_al[kH + h0 + i] * u2f(o1[i]);
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) acc0[i] = acc1[i] = 0.0f;
+      for (int k = 0; k <= np && okm; ++k) {
+        const int pr = (k - 1) & 1;
+        if (k > 0 && !wait_all(mbar_wait(merge_bar(1 + pr), ((k - 1) >> 1) & 1, kWaitNs))) {
+          okm = false;
+          break;
         }
-        for (int k = 1; k <= np; ++k, ++uses) {
-          const int pr = uses & 1;
-          if (!wait_all(mbar_wait(merge_bar(1 + pr), (uses >> 1) & 1, kWaitNs))) {
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {  // (16-head chunk, d_v half)
+          const int h0 = hb + 16 * (q >> 1), half = q & 1;
+          const uint32_t tc = tl + O_COL + 64 * half + h0;
+          uint32_t o[16];
+          if (k > 0 || had) {
+            tmem_ld32_x16(tc, o);
+            tc_wait_ld();
+          }
+          if (k == 0) {
+            const float* w = red_al + half * kH + h0;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] = f2u(had ? w[i] * u2f(o[i]) : 0.0f);
+          } else {
+            const uint8_t* r = smem + (slot(pr, half) - sbase) + tr * 256;
+            const float* w = red_wk + (half * kMaxParts + k - 1) * kH + h0;
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) {
+              const float4 x = *reinterpret_cast<const float4*>(r + 16 * ((((h0 + i) >> 2) ^ tr) & 15));
+              o[i] = f2u(fmaf(w[i], x.x, u2f(o[i])));
+              o[i + 1] = f2u(fmaf(w[i + 1], x.y, u2f(o[i + 1])));
+              o[i + 2] = f2u(fmaf(w[i + 2], x.z, u2f(o[i + 2])));
+              o[i + 3] = f2u(fmaf(w[i + 3], x.w, u2f(o[i + 3])));
+            }
+          }
+          if (k == np) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) stage[(h0 + i) * kD + 128 * half + tr] = __bfloat16_as_ushort(__float2bfloat16_rn(u2f(o[i])));
+          } else {
+            tmem_st32_x16(tc, o);
+          }
+        }
+        if (k < np) tc_wait_st();  // the next step reads these columns back
+        if (k >= 1 && k + 2 <= np) {
+          // every warp has read this slot pair: refill it with part k + 2
+          if (xsync(false) < 0) {
             okm = false;
             break;
           }
-          const uint8_t* r0 = smem + (slot(pr, 0) - sbase) + tr * 256;
-          const uint8_t* r1 = smem + (slot(pr, 1) - sbase) + tr * 256;
-          const float* wk0 = red_wk + (k - 1) * kH + h0;
-          const float* wk1 = red_wk + (kMaxParts + k - 1) * kH + h0;
-#pragma unroll
-          for (int i = 0; i < 16; i += 4) {
-            const int pos = 16 * ((((h0 + i) >> 2) ^ tr) & 15);
-            const float4 x = *reinterpret_cast<const float4*>(r0 + pos);
-            const float4 y = *reinterpret_cast<const float4*>(r1 + pos);
-            acc0[i] += wk0[i] * x.x;
-            acc0[i + 1] += wk0[i + 1] * x.y;
-            acc0[i + 2] += wk0[i + 2] * x.z;
-            acc0[i + 3] += wk0[i + 3] * x.w;
-            acc1[i] += wk1[i] * y.x;
-            acc1[i + 1] += wk1[i + 1] * y.y;
-            acc1[i + 2] += wk1[i + 2] * y.z;
-            acc1[i + 3] += wk1[i + 3] * y.w;
+          if (sid == 0) {
+            fence_proxy_async_smem();
+            fetch_part(k + 2);
           }
-          // the fill two ahead: the next part of this chunk's pass, or of the second chunk's
-          const int ahead = uses + 2, total = np > 2 ? 2 * np : np;
-          if (ahead < total) {
-            // every warp has read this slot pair: refill it
-            if (xsync(false) < 0) {
-              okm = false;
-              break;
-            }
-            if (sid == 0) {
-              fence_proxy_async_smem();
-              fetch_part(ahead);
-            }
-          }
-        }
-        if (!okm) break;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          stage[(h0 + i) * kD + tr] = __bfloat16_as_ushort(__float2bfloat16_rn(acc0[i]));
-          stage[(h0 + i) * kD + 128 + tr] = __bfloat16_as_ushort(__float2bfloat16_rn(acc1[i]));
         }
       }
       if (!okm) break;
