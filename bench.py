@@ -97,7 +97,7 @@ def kernels_per_call(wl, sm_count):
         return 1
     nt = (wl.indices.shape[1] + 127) // 128
     u = wl.T * nt
-    g = min(sm_count, (u + 3) // 4)
+    g = min(sm_count, (u + 1) // 2)
     while g > 1 and (nt + u // g - 1) // (u // g) + 1 > 17:
         g -= 1
     gap = (nt + 14) // 15
@@ -521,9 +521,60 @@ def measure(args, wl, rank, world, device, config=None):
     }
 
 
+def measure_latency(args, wl, device):
+    """Device time of one call on a small batch, L2 flushed before each: replayed from a CUDA
+    graph (the kernels alone, no host marshalling between the events) and launched directly
+    (host marshalling included, as one isolated call sees it)."""
+    import torch
+
+    import dsa_sparse_attention_mla_gb300 as dsa
+
+    q, cache, idx, bt, req = build_device_inputs(wl, device)
+    out = torch.empty((wl.T, wl.H, wl.d_v), dtype=torch.bfloat16, device=device)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    ws = torch.zeros(dsa.dsa_sparse_attn_workspace_size(wl.d_v), dtype=torch.uint8, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    s = torch.cuda.Stream(device)
+
+    def step():
+        dsa.dsa_sparse_attn(q, cache, wl.kind, idx, wl.sm_scale, d_nope=wl.d_nope, d_rope=wl.d_rope, d_v=wl.d_v,
+                            block_table=bt, page_size=wl.page_size, req_of_token=req, out=out, workspace=ws,
+                            error_word=err)
+
+    n = max(10, min(args.steps, 200))
+    with torch.cuda.stream(s):
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize(device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            step()
+        torch.cuda.synchronize(device)
+        res = {}
+        for mode in ("graph", "launch"):
+            ts = []
+            for i in range(n):
+                flush.fill_(i & 0xFF)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(s)
+                g.replay() if mode == "graph" else step()
+                b.record(s)
+                torch.cuda.synchronize(device)
+                ts.append(a.elapsed_time(b) * 1000.0)
+            res[mode] = statistics.median(ts)
+    if err.item() != 0:
+        raise RuntimeError(f"device error word {err.item()} during the latency measurement")
+    work = algorithmic_work(wl)
+    return {"workload": wl.name, "tokens": wl.T, "us_per_call_graph": res["graph"], "us_per_call_launch": res["launch"],
+            "calls": n, "roofline_us": max(work["unique_bytes"] / (_peaks()[0] * 1e9),
+                                           work["flops"] / (_peaks()[1] * 1e12)) * 1e6,
+            "gpu_launches_per_call": kernels_per_call(wl, torch.cuda.get_device_properties(device).multi_processor_count)}
+
+
 def workload_config(wl, work):
     return {"workload": wl.name, "tokens_per_step": wl.T, "heads": wl.H, "d_nope": wl.d_nope, "d_rope": wl.d_rope,
-            "d_v": wl.d_v, "topk": wl.topk, "valid_entries": work["n_valid"], "cache": "fp8_264B" if wl.kind else "bf16",
+            "d_v": wl.d_v, "topk": wl.topk, "valid_entries": work["n_valid"],
+            "cache": f"fp8_{wl.d_nope + 4 * (wl.d_nope // 128) + 2 * wl.d_rope}B" if wl.kind else "bf16",
             "slots": wl.num_slots, "page_size": wl.page_size or None,
             "l2": f"{L2_FLUSH_BYTES >> 20} MB buffer written between timed steps (outside the events)"}
 
@@ -540,6 +591,8 @@ def main():
                     help="requant: time dsa_gather_requant on the decode workload's rows instead")
     ap.add_argument("--no-prefill", dest="prefill", action="store_false",
                     help="with the default decode workload, skip the second (T=8192 prefill) measurement")
+    ap.add_argument("--no-extra", dest="extra", action="store_false",
+                    help="with the default decode workload, skip the 512+64 control and small-batch latency")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -608,6 +661,17 @@ def main():
             line["prefill"] = {k: sub[k] for k in ("metric", "value", "unit", "ms_per_step", "dtype", "config",
                                                    "roofline", "cpu_baseline", "e2e", "gpu_launches", "clocks",
                                                    "step_ms")}
+    if args.config == 3 and args.extra:
+        # the 512+64 control (FP8 656-byte rows, T=1024), timed like the headline workload
+        wl5 = W.config(5, seed=0)
+        sub = measure(args, wl5, rank, world, device, config=5)
+        if line is not None and sub is not None:
+            line["control"] = {k: sub[k] for k in ("metric", "value", "unit", "ms_per_step", "dtype", "config",
+                                                   "roofline", "cpu_baseline", "e2e", "gpu_launches", "clocks",
+                                                   "step_ms")}
+        # small batches (T=17 BF16 direct, T=8 FP8 paged): device time per call
+        if rank == 0 and line is not None:
+            line["small_batch"] = [measure_latency(args, W.config(c, seed=0), device) for c in (1, 2)]
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()

@@ -207,6 +207,19 @@ def test_many_tokens_stream_split(gpu):
         _check(wl, gpu)
 
 
+@pytest.mark.parametrize("kind", [0, 1])
+@pytest.mark.parametrize("T", [2, 37, 74, 150])
+def test_split_token_merge_part_counts(gpu, kind, T):
+    """Batches whose tokens split into about eight, four, two and one extra part(s): the head
+    CTA's merge streams every part through its two shared-memory slot pairs (more than two
+    parts reuse them) and adds them in a fixed order."""
+    wl = W.fp8_paged(T=T, requests=2, positions=4096, page_size=64, topk=2048, n_valid=2000, seed=60 + T,
+                     sm_scale=1 / 16, scatter_frac=0.3)
+    if kind == 0:
+        wl.kind = 0
+    _check(wl, gpu)
+
+
 def test_strided_q_and_out(gpu):
     wl = W.bf16_direct(T=5, slots=3000, topk=2048, n_valid=2048, seed=14, sm_scale=1 / 16)
     cache = oracle_cache(wl)
