@@ -36,7 +36,9 @@
 //    accumulator. Half t is normalised by 2^(m'_t - m - 4) / l at the token's end.
 //  * Persistent cooperative launch, one CTA per SM; (token, 128-position tile) units split into
 //    contiguous ranges per CTA; a token cut by a range boundary is merged in-kernel by the CTA
-//    holding its first tiles (fixed order, no atomics on data).
+//    holding its first tiles: the other parts' partial results come into idle shared memory by
+//    bulk copies (two in flight) and are added, in a fixed order, into its O columns of tensor
+//    memory (no atomics on data).
 //  * Warp roles: 0 producer (index read, -1 compaction into dense 128-key tiles, page
 //    translation), 1 score-MMA issuer, 2 output-MMA issuer, 4-11 softmax, query split and
 //    epilogue (two warps per TMEM lane quarter, 32 heads each), 3 and 12-15 row loaders (which
