@@ -425,6 +425,88 @@ def run_requant(args, device):
     print(json.dumps(line))
 
 
+def run_proj(args, device):
+    """Timing of the FP8 block-scaled projection GEMM at prefill size (8192 tokens): q_b_proj
+    (K 2048 -> N 16384 = 64 heads x 256) and o_proj (K 16384 -> N 6144); the pages name the layers
+    but give no widths, so these are read from the attention's geometry. Weights are quantised
+    once; each timed step quantises the activations (1 x 128 blocks) and runs the GEMM. Bound:
+    the FP8 tensor peak, taken as twice the measured bf16 burst (the nominal 4.5 / 2.25 ratio)."""
+    import torch
+
+    import dsa_sparse_attention_mla_gb300 as dsa
+
+    M = 8192
+    shapes = [("q_b_proj", 2048, 16384), ("o_proj", 16384, 6144)]
+    gen = torch.Generator(device=device).manual_seed(0)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    fp8_peak = 2.0 * _peaks()[1]
+    out = []
+    for name, K, N in shapes:
+        x = torch.randn((M, K), generator=gen, device=device).to(torch.bfloat16)
+        w = (torch.randn((N, K), generator=gen, device=device) * 0.02).to(torch.bfloat16)
+        wc, ws = dsa.dsa_quant_fp8_blockscale(w, 128)
+        xc = torch.empty((M, K), dtype=torch.uint8, device=device)
+        xs = torch.empty(dsa.dsa_blockscale_bytes(M, K), dtype=torch.uint8, device=device)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+
+        def step():
+            dsa.dsa_quant_fp8_blockscale(x, 1, codes=xc, scales=xs)
+            dsa.dsa_proj_gemm(xc, xs, wc, ws, out=y)
+
+        for _ in range(args.warmup):
+            flush.fill_(1)
+            step()
+        torch.cuda.synchronize(device)
+        n = max(3, min(args.steps, 200))
+        t_all, t_gemm = [], []
+        with ClockSampler(device) as clk:
+            for i in range(n):
+                flush.fill_(i & 0xFF)
+                a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+                a.record(stream)
+                dsa.dsa_quant_fp8_blockscale(x, 1, codes=xc, scales=xs)
+                b.record(stream)
+                dsa.dsa_proj_gemm(xc, xs, wc, ws, out=y)
+                c.record(stream)
+                torch.cuda.synchronize(device)
+                t_all.append(a.elapsed_time(c))
+                t_gemm.append(b.elapsed_time(c))
+        ms, ms_g = statistics.median(t_all), statistics.median(t_gemm)
+        flops = 2.0 * M * N * K
+        out.append({"layer": name, "M": M, "K": K, "N": N, "ms_per_step": ms, "gemm_ms": ms_g,
+                    "tflops": flops / (ms / 1e3) / 1e12, "gemm_tflops": flops / (ms_g / 1e3) / 1e12,
+                    "roofline": {"bound": "tensor", "achieved": flops / (ms_g / 1e3) / 1e12, "peak": fp8_peak,
+                                 "unit": "TFLOP/s", "frac": flops / (ms_g / 1e3) / 1e12 / fp8_peak,
+                                 "peak_source": "2 x measured bf16 burst"},
+                    "clocks": clk.summary()})
+    # CPU baseline: the oracle's product on a sample of 4 rows of the first layer
+    from oracle import projection as P
+
+    K, N = shapes[0][1], 256
+    rng = np.random.default_rng(0)
+    xb = P.f64_to_bf16(rng.standard_normal((4, K)))
+    wb = P.f64_to_bf16(rng.standard_normal((N, K)) * 0.02)
+    xc_h, xe_h = P.quant_blockscale(xb, 1)
+    wc_h, we_h = P.quant_blockscale(wb, 128)
+    t0 = time.perf_counter()
+    P.proj_gemm(xc_h, xe_h, wc_h, we_h)
+    cpu = 2.0 * 4 * N * K / (time.perf_counter() - t0)
+    tot_flops = sum(2.0 * M * o["N"] * o["K"] for o in out)
+    tot_ms = sum(o["ms_per_step"] for o in out)
+    line = {"metric": "FP8 block-scaled projection GEMM TFLOP/s (q_b_proj + o_proj, 8192 tokens)",
+            "value": tot_flops / (tot_ms / 1e3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1, "steps": n,
+            "warmup": args.warmup, "ms_per_step": tot_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+            "config": {"workload": "fp8_blockscale_proj_M8192", "layers": out,
+                       "l2": f"{L2_FLUSH_BYTES >> 20} MB buffer written between timed steps (outside the events)"},
+            "cpu_baseline": {"value": cpu / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                             "sample": "4 rows x 256 columns of q_b_proj (fp64 numpy product, quantisation excluded)",
+                             "cpu": cpu_model()},
+            "gpu_launches": n * 2 * len(shapes)}
+    print(json.dumps(line))
+
+
 # ---------------------------------------------------------------------------- CPU oracle --
 class OracleRunner:
     """The CPU oracle (as it stands) on the workload. The packed cache rows the tokens name are
@@ -587,8 +669,9 @@ def main():
     ap.add_argument("--config", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--op", default="attn", choices=["attn", "requant"],
-                    help="requant: time dsa_gather_requant on the decode workload's rows instead")
+    ap.add_argument("--op", default="attn", choices=["attn", "requant", "proj"],
+                    help="requant: time dsa_gather_requant on the decode workload's rows instead; proj: the "
+                         "FP8 block-scaled projection GEMM")
     ap.add_argument("--no-prefill", dest="prefill", action="store_false",
                     help="with the default decode workload, skip the second (T=8192 prefill) measurement")
     ap.add_argument("--no-extra", dest="extra", action="store_false",
@@ -645,9 +728,9 @@ def main():
     __graft_entry__.build() if rank == 0 else None
     if world > 1:
         torch.distributed.barrier()
-    if args.op == "requant":
+    if args.op in ("requant", "proj"):
         if rank == 0:
-            run_requant(args, device)
+            (run_requant if args.op == "requant" else run_proj)(args, device)
         if world > 1:
             torch.distributed.destroy_process_group()
         return

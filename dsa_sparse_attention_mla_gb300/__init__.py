@@ -97,6 +97,12 @@ def load_library():
         lib.dsa_sparse_attn_static_ws.restype = i32
         lib.dsa_topk_select.argtypes = [P, i64, i64, i64, P, i32, P, i64, P]
         lib.dsa_topk_select.restype = i32
+        lib.dsa_blockscale_bytes.argtypes = [i64, i64]
+        lib.dsa_blockscale_bytes.restype = i64
+        lib.dsa_quant_fp8_blockscale.argtypes = [P, i64, i64, i64, i32, P, P, P]
+        lib.dsa_quant_fp8_blockscale.restype = i32
+        lib.dsa_proj_gemm.argtypes = [P, P, P, P, i64, i64, i64, P, i64, P, ctypes.c_size_t, P]
+        lib.dsa_proj_gemm.restype = i32
         _LIB = lib
         return lib
 
@@ -378,4 +384,78 @@ def dsa_topk_select(scores, K: int, *, lengths=None, out=None):
     st = load_library().dsa_topk_select(_ptr(scores), T, S, scores.stride(0), _ptr(lengths), int(K), _ptr(out),
                                         out.stride(0), _stream(scores.device))
     _check(st, "dsa_topk_select")
+    return out
+
+
+def dsa_blockscale_bytes(rows: int, cols: int) -> int:
+    return int(load_library().dsa_blockscale_bytes(rows, cols))
+
+
+def dsa_quant_fp8_blockscale(x, block_rows: int, *, codes=None, scales=None):
+    """(codes uint8 [R, C], scales uint8 [dsa_blockscale_bytes(R, C)]) of bf16 x [R, C]: e4m3 codes
+    with one power-of-two scale per block_rows x 128 block (128: weights, 1: activations), the
+    scales in the projection GEMM's block-scale layout."""
+    import torch
+
+    _need_cuda("x", x, torch.bfloat16)
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be [rows, cols], contiguous along cols")
+    R, C = x.shape
+    nb = dsa_blockscale_bytes(R, C)
+    if nb < 0:
+        raise ValueError("cols must be a positive multiple of 128")
+    if codes is None:
+        codes = torch.empty((R, C), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(nb, dtype=torch.uint8, device=x.device)
+    _need_cuda("codes", codes, torch.uint8)
+    _need_cuda("scales", scales, torch.uint8)
+    if tuple(codes.shape) != (R, C) or not codes.is_contiguous() or scales.numel() < nb or not scales.is_contiguous():
+        raise ValueError("codes must be contiguous [rows, cols] and scales hold dsa_blockscale_bytes(rows, cols)")
+    st = load_library().dsa_quant_fp8_blockscale(_ptr(x), R, C, x.stride(0), int(block_rows), _ptr(codes), _ptr(scales),
+                                                 _stream(x.device))
+    _check(st, "dsa_quant_fp8_blockscale")
+    return codes, scales
+
+
+_GEMM_WS = {}
+
+
+def _gemm_workspace(device, nbytes: int = 32 << 20):
+    """The GEMM's scratch for the current stream on ``device`` (its own buffer: the attention's
+    default workspace must keep its flags)."""
+    import torch
+
+    index = device.index if device.index is not None else torch.cuda.current_device()
+    key = (index, torch.cuda.current_stream(index).cuda_stream)
+    with _lock:
+        ws = _GEMM_WS.get(key)
+        if ws is None:
+            ws = torch.empty(nbytes, dtype=torch.uint8, device=torch.device("cuda", index))
+            _GEMM_WS[key] = ws
+    return ws
+
+
+def dsa_proj_gemm(x_codes, x_scales, w_codes, w_scales, *, out=None, workspace=None):
+    """bf16 [M, N] = X W^T over block-scaled FP8 operands (x from block_rows=1 [M, K], w from
+    block_rows=128 [N, K])."""
+    import torch
+
+    for name, t in (("x_codes", x_codes), ("x_scales", x_scales), ("w_codes", w_codes), ("w_scales", w_scales)):
+        _need_cuda(name, t, torch.uint8)
+    M, K = x_codes.shape
+    N, K2 = w_codes.shape
+    if K2 != K:
+        raise ValueError("x and w must share K")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x_codes.device)
+    _need_cuda("out", out, torch.bfloat16)
+    if out.dim() != 2 or tuple(out.shape) != (M, N) or out.stride(1) != 1:
+        raise ValueError("out must be [M, N] bf16, contiguous along N")
+    if workspace is None:
+        workspace = _gemm_workspace(x_codes.device)
+    _need_cuda("workspace", workspace, torch.uint8)
+    st = load_library().dsa_proj_gemm(_ptr(x_codes), _ptr(x_scales), _ptr(w_codes), _ptr(w_scales), M, N, K, _ptr(out),
+                                      out.stride(0), _ptr(workspace), workspace.numel(), _stream(x_codes.device))
+    _check(st, "dsa_proj_gemm")
     return out

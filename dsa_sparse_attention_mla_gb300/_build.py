@@ -1,7 +1,8 @@
 """Build the CUDA library in-tree: csrc/*.cu -> libdsa_gb300.so (sm_103a only).
 
 Each translation unit is compiled by its own nvcc process (in parallel), then linked with
-``nvcc -shared``. The CUDA runtime is linked statically, so the library only needs the driver.
+``nvcc -shared``. The CUDA runtime is linked statically; besides the driver the library needs
+cuBLASLt (the projection GEMM), found in the toolkit's lib64 by an rpath.
 """
 from __future__ import annotations
 
@@ -74,7 +75,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(cmds), os.cpu_count() or 4))) as ex:
         list(ex.map(run, cmds))
     tmp = LIB_PATH + f".tmp{os.getpid()}"
-    run([nvcc, "-shared", "-gencode", "arch=compute_103a,code=sm_103a", "-o", tmp, *objs])
+    # the projection GEMM calls cuBLASLt (a plain library GEMM): link it from the toolkit nvcc
+    # belongs to, and find it there at run time
+    libdir = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc))), "lib64")
+    run([nvcc, "-shared", "-gencode", "arch=compute_103a,code=sm_103a", "-o", tmp, *objs, "-L", libdir, "-lcublasLt",
+         "-Xlinker", "-rpath", "-Xlinker", libdir])
     os.replace(tmp, LIB_PATH)
     return LIB_PATH
 

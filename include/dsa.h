@@ -242,6 +242,39 @@ DSA_API dsa_status_t dsa_sparse_attn(const dsa_attn_args_t* args, void* stream);
  */
 DSA_API dsa_status_t dsa_sparse_attn_static_ws(const dsa_attn_args_t* args, void* stream);
 
+/*
+ * FP8 block-scaled projection GEMM, for the dense MLA projections around the attention
+ * (sglang PR #31955 "Opt-in prefill-only FP8 dense projection GEMM for MLA q_b/o_proj",
+ * Motivation and Modifications: weights repacked into e4m3 with one UE8M0 (power-of-two) scale
+ * per 128x128 block, activations quantised per token and 128-column group, "a8w8 blockscale").
+ *
+ * dsa_blockscale_bytes - bytes of the scale tensor of a [rows, cols] matrix (cols a multiple of
+ * 128): ceil(rows / 128) * (cols / 128) * 512; -1 for invalid sizes.
+ *
+ * dsa_quant_fp8_blockscale - quantise bf16 x [rows, cols] (row stride in elements, a multiple
+ * of 8; cols a multiple of 128) into e4m3 codes [rows, cols] (uint8, contiguous) and scales.
+ * block_rows = 128 (weights: 128 x 128 blocks) or 1 (activations: 1 x 128 blocks). Per block,
+ * e = the smallest integer in [-127, 127] with 448 * 2^e >= max |x| (0 for an all-zero block) and
+ * code = e4m3 round-to-nearest-even of x / 2^e (exact; nothing saturates). The UE8M0 bytes e + 127
+ * are stored in the GEMM's 32-element block-scale layout: each 128-column block is four equal
+ * 32-column scales; tiles of 128 rows x 4 scale columns (512 bytes; row r, scale column c at
+ * (r % 32) * 16 + ((r % 128) / 32) * 4 + c % 4) in row-tile-major order. Scales of rows past
+ * `rows` in the last tile read 127 (scale 1). Inputs must be finite. Pointers 16-byte aligned.
+ *
+ * dsa_proj_gemm - y[m, n] = sum_k x[m, k] w[n, k] over the dequantised operands (x from
+ * block_rows = 1, w [N, K] from block_rows = 128), fp32 accumulation, bf16 output y [M, N] with
+ * row stride y_stride (elements, a multiple of 8). N and K multiples of 128. The product runs in
+ * cuBLASLt (e4m3 operands with 32-element UE8M0 block scales); `workspace` (256-byte aligned,
+ * may be NULL with workspace_bytes 0) is its scratch. Calls on one device are serialised on the
+ * host (the library keeps one cuBLASLt handle and a plan cache per device).
+ */
+DSA_API int64_t dsa_blockscale_bytes(int64_t rows, int64_t cols);
+DSA_API dsa_status_t dsa_quant_fp8_blockscale(const void* x, int64_t rows, int64_t cols, int64_t row_stride,
+                                              int block_rows, void* codes, void* scales, void* stream);
+DSA_API dsa_status_t dsa_proj_gemm(const void* x_codes, const void* x_scales, const void* w_codes,
+                                   const void* w_scales, int64_t M, int64_t N, int64_t K, void* y, int64_t y_stride,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

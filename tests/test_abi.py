@@ -20,7 +20,7 @@ def _declared():
 def test_header_declares_the_entry_points():
     names = _declared()
     for n in ["dsa_quant_k_cache", "dsa_gather_dequant", "dsa_gather_requant", "dsa_sparse_attn", "dsa_sparse_attn_workspace_size",
-              "dsa_topk_select",
+              "dsa_topk_select", "dsa_quant_fp8_blockscale", "dsa_proj_gemm", "dsa_blockscale_bytes",
               "dsa_packed_row_bytes", "dsa_cache_row_bytes", "dsa_status_string", "dsa_last_cuda_error"]:
         assert n in names
 
@@ -102,3 +102,19 @@ def test_argument_errors_need_no_gpu(dsa_lib):
     b = dsa.DsaAttnArgs.from_buffer_copy(good)
     b.T = 0
     assert L.dsa_sparse_attn(ctypes.byref(b), None) == 0
+
+
+def test_blockscale_sizes_and_argument_errors(dsa_lib):
+    assert dsa.dsa_blockscale_bytes(1, 128) == 512
+    assert dsa.dsa_blockscale_bytes(129, 256) == 2 * 2 * 512
+    assert dsa.dsa_blockscale_bytes(8, 100) == -1
+    P = ctypes.c_void_p(16)
+    # bad block size, cols not a multiple of 128: rejected before any device work
+    assert dsa_lib.dsa_quant_fp8_blockscale(P, 4, 128, 128, 7, P, P, None) == 1
+    assert dsa_lib.dsa_quant_fp8_blockscale(P, 4, 100, 128, 1, P, P, None) == 1
+    assert dsa_lib.dsa_quant_fp8_blockscale(P, 4, 128, 120, 1, P, P, None) == 1
+    # N and K multiples of 128, output stride at least N
+    assert dsa_lib.dsa_proj_gemm(P, P, P, P, 4, 100, 128, P, 128, None, 0, None) == 1
+    assert dsa_lib.dsa_proj_gemm(P, P, P, P, 4, 128, 100, P, 128, None, 0, None) == 1
+    assert dsa_lib.dsa_proj_gemm(P, P, P, P, 4, 256, 128, P, 128, None, 0, None) == 1
+    assert dsa_lib.dsa_proj_gemm(P, P, P, P, 0, 128, 128, P, 128, None, 0, None) == 0
