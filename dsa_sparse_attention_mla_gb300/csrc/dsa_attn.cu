@@ -1043,7 +1043,6 @@ static dsa_status_t launch(const dsa_attn_args_t* a, const DeviceInfo& dev, cuda
 }
 
 using CfgBf16_576 = AttnCfg<DSA_CACHE_BF16, 512, 64, 2, 64, 2>;
-using CfgFp8_576 = AttnCfg<DSA_CACHE_FP8_SCALED, 512, 64, 2, 64, 2>;
 
 dsa_status_t prepare_attn_kernels(int device) {
   static std::mutex mu;
@@ -1054,9 +1053,9 @@ dsa_status_t prepare_attn_kernels(int device) {
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(dsa_attn_kernel<CfgBf16_576>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 CfgBf16_576::SMEM_BYTES)) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(dsa_attn_kernel<CfgFp8_576>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                CfgFp8_576::SMEM_BYTES)) != cudaSuccess ||
-      (e = k128_set_attributes()) != cudaSuccess || (e = f8_set_attributes()) != cudaSuccess)
+
+      (e = k128_set_attributes()) != cudaSuccess || (e = f8_set_attributes()) != cudaSuccess ||
+      (e = ctl_set_attributes()) != cudaSuccess)
     return cuda_fail(e);
   done[device] = true;
   return DSA_OK;
@@ -1118,8 +1117,8 @@ dsa_status_t dsa_sparse_attn(const dsa_attn_args_t* a, void* stream) {
   if (st != DSA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (a->d_nope == 256) return launch_attn_k128(a, dev, s);
-  if (a->kind == DSA_CACHE_BF16) return launch<CfgBf16_576>(a, dev, s);
-  return launch<CfgFp8_576>(a, dev, s);
+  if (a->kind == DSA_CACHE_FP8_SCALED) return launch_attn_ctl(a, dev, s);
+  return launch<CfgBf16_576>(a, dev, s);
 }
 
 }  // extern "C"
@@ -1184,6 +1183,6 @@ extern "C" dsa_status_t dsa_sparse_attn_static_ws(const dsa_attn_args_t* a, void
   // nothing needs clearing: the array starts zero-filled and each call tags its merge flags
   // with a fresh per-array epoch, so values left by an earlier call never match
   if (b.d_nope == 256) return launch_attn_k128(&b, capped, s);
-  if (b.kind == DSA_CACHE_BF16) return launch<CfgBf16_576>(&b, capped, s);
-  return launch<CfgFp8_576>(&b, capped, s);
+  if (b.kind == DSA_CACHE_FP8_SCALED) return launch_attn_ctl(&b, capped, s);
+  return launch<CfgBf16_576>(&b, capped, s);
 }

@@ -59,6 +59,11 @@ cudaError_t f8_set_attributes();
 // bf16 rows the keys-as-M bf16 kernel (dsa_attn_k128.cu).
 dsa_status_t launch_attn_f8(const dsa_attn_args_t* a, const DeviceInfo& dev, cudaStream_t stream);
 
+// The 512+64 control geometry over packed FP8 rows: keys-as-M with 8-bit operands, 32 heads per
+// work unit (dsa_attn_ctl.cu).
+cudaError_t ctl_set_attributes();
+dsa_status_t launch_attn_ctl(const dsa_attn_args_t* a, const DeviceInfo& dev, cudaStream_t stream);
+
 // Keys-as-M kernel for the 256+0 latent geometry (dsa_attn_k128.cu); routes packed FP8 rows
 // to launch_attn_f8.
 dsa_status_t launch_attn_k128(const dsa_attn_args_t* a, const DeviceInfo& dev, cudaStream_t stream);
