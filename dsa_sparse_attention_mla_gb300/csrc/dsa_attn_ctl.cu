@@ -85,7 +85,7 @@ constexpr int RED_OFF = CMP_OFF + 4 * 256;
 constexpr int RED_FLOATS = kH + 4 * kH + 4 * kH + 5 * kH + 4 * kH + 16 + kH + 2 * kNSM;
 enum : int {
   B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_KEMPTY = B_KFULL + kKST, B_REMPTY = B_KEMPTY + kKST,
-  B_MFULL = B_REMPTY + 1, B_MEMPTY = B_MFULL + kMST, B_SFULL = B_MEMPTY + kMST, B_SEMPTY = B_SFULL + 2,
+  B_RFULL = B_REMPTY + 1, B_MFULL = B_RFULL + 1, B_MEMPTY = B_MFULL + kMST, B_SFULL = B_MEMPTY + kMST, B_SEMPTY = B_SFULL + 2,
   B_PFULL = B_SEMPTY + 2, B_PVDONE = B_PFULL + 1, B_XBAR = B_PVDONE + 2, B_DRAIN = B_XBAR + 1,
   B_RANGE = B_DRAIN + 2, B_MERGE = B_RANGE + 1, NBARS = B_MERGE + 3
 };
@@ -253,6 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_ctl_kernel(const __grid_cons
   auto k_full = [&](int s) { return bar(B_KFULL + s); };
   auto k_empty = [&](int s) { return bar(B_KEMPTY + s); };
   const uint32_t r_empty = bar(B_REMPTY);  // the RoPE buffer: the score products that read it are complete
+  const uint32_t r_full = bar(B_RFULL);    // the RoPE buffer holds the current tile's rows
   auto m_full = [&](int s) { return bar(B_MFULL + s); };
   auto m_empty = [&](int s) { return bar(B_MEMPTY + s); };
   auto s_full = [&](int i) { return bar(B_SFULL + i); };
@@ -276,6 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_ctl_kernel(const __grid_cons
       mbar_init(k_empty(s), 1);
     }
     mbar_init(r_empty, 1);
+    mbar_init(r_full, 32 * kNLD);
     for (int s = 0; s < kMST; ++s) {
       mbar_init(m_full(s), 1);
       mbar_init(m_empty(s), 2 + kNSM + kNLD);
@@ -533,6 +535,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_ctl_kernel(const __grid_cons
               mma_f8_lohi<1>(d0 + 32 * t, ka, k_hi, qa + (4096 >> 4), k_hi, idS);
             }
           }
+          if (!wait(r_full, g & 1)) break;
+          fence_proxy_async_smem();
+          tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             if (kk == 0) mma_bf16_lohi<0>(d0 + 128, kr_lo, k_hi, qr_lo, k_hi, idR);
@@ -1034,9 +1039,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_ctl_kernel(const __grid_cons
     }
   } else {
     // ================================================= row loaders (warps 3, 12-15) ====
-    // Row k of a tile goes to loader k % 5; per row, 32 lanes copy its 512 codes (granule l of
-    // the row: chunk l / 8 of the stage, position l % 8), then lanes 0-7 its 128 RoPE bytes and
-    // lane 8 its four scales. Rows past the tile's valid count are zero-filled.
+    // Row k of a tile goes to loader k % 5, whose lane k / 5 holds its slot. Per tile, first the
+    // codes into the free stage (one instruction per row: granule l of the row goes to chunk
+    // l / 8, position l % 8) and the four scales of each row (one instruction for all the warp's
+    // rows), signalled on k_full; then, once the previous tile's score products have read the
+    // RoPE buffer, the 128 RoPE bytes of each row (four rows per instruction), signalled on
+    // r_full. The codes of the next tile thus stream in while the current one is scored. Rows
+    // past the tile's valid count are zero-filled.
     const int li = warp == 3 ? 0 : warp - 11;
     const int nrow = (kBN - li + kNLD - 1) / kNLD;  // rows li + 5 k, k < nrow
     uint32_t mc = 0, g = 0;
@@ -1047,10 +1056,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_ctl_kernel(const __grid_cons
       const MetaHdr* mh = reinterpret_cast<const MetaHdr*>(smem + META_OFF + st * META_BYTES);
       const int type = mh->type;
       int n = 0, slr = -1;
+      const int rt = li + kNLD * lane;
       if (type == kTile) {
         n = mh->n_valid;
         const int* slots = reinterpret_cast<const int*>(reinterpret_cast<const uint8_t*>(mh) + META_HDR);
-        const int rt = li + kNLD * lane;
         if (lane < nrow && rt < n) slr = slots[rt];
       }
       __syncwarp();
@@ -1060,28 +1069,40 @@ __global__ void __launch_bounds__(kThreads, 1) attn_ctl_kernel(const __grid_cons
       if (type != kTile) continue;
       const int ks = g % kKST;
       if (g >= (uint32_t)kKST && !wait(k_empty(ks), ((g / kKST) & 1) ^ 1)) break;
-      if (g >= 1 && !wait(r_empty, (g - 1) & 1)) break;  // the RoPE buffer's previous tile is scored
       const uint32_t kt = sbase + KT_OFF + ks * KT_BYTES;
       const uint32_t kr = sbase + KR_OFF;
       const uint32_t scs = sbase + SC_OFF + ks * SC_BYTES;
-#pragma unroll 1
+#pragma unroll 2
       for (int k = 0; k < nrow; ++k) {
         const int r = li + kNLD * k;
         const int sl = __shfl_sync(0xffffffffu, slr, k);
         const uint8_t* row = p.cache + (int64_t)(sl >= 0 ? sl : 0) * kRB;
-        const uint32_t sz = sl >= 0 ? 16 : 0;
         const uint32_t dst = kt + (lane >> 3) * (kBN * 128) + r * 128 + (((lane & 7) ^ (r & 7)) << 4);
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(row + 16 * lane), "r"(sz) : "memory");
-        if (lane < 8) {
-          const uint32_t dr = kr + r * 128 + ((lane ^ (r & 7)) << 4);
-          asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dr), "l"(row + kD + 16 + 16 * lane), "r"(sz)
-                       : "memory");
-        } else if (lane == 8) {
-          asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(scs + r * 16), "l"(row + kD), "r"(sz)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(row + 16 * lane), "r"(sl >= 0 ? 16 : 0)
+                     : "memory");
+      }
+      if (lane < nrow) {
+        const uint8_t* row = p.cache + (int64_t)(slr >= 0 ? slr : 0) * kRB;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(scs + rt * 16), "l"(row + kD),
+                     "r"(slr >= 0 ? 16 : 0)
+                     : "memory");
+      }
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(k_full(ks)) : "memory");
+      if (g >= 1 && !wait(r_empty, (g - 1) & 1)) break;  // the RoPE buffer's previous tile is scored
+      // four rows per instruction: lane 8 j + i copies granule i of row 4 k4 + j
+#pragma unroll 1
+      for (int k4 = 0; k4 < nrow; k4 += 4) {
+        const int k = k4 + (lane >> 3), gi = lane & 7;
+        const int sl = __shfl_sync(0xffffffffu, slr, k & 31);
+        if (k < nrow) {
+          const int r = li + kNLD * k;
+          const uint8_t* row = p.cache + (int64_t)(sl >= 0 ? sl : 0) * kRB;
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(kr + r * 128 + ((gi ^ (r & 7)) << 4)),
+                       "l"(row + kD + 16 + 16 * gi), "r"(sl >= 0 ? 16 : 0)
                        : "memory");
         }
       }
-      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(k_full(ks)) : "memory");
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(r_full) : "memory");
       ++g;
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
