@@ -116,6 +116,15 @@ def test_control_512_64(gpu, kind, T):
     _check(wl, gpu)
 
 
+@pytest.mark.parametrize("T,topk,n_valid", [(1, 4096, 4096), (1, 4224, 4100), (3, 4096, 3001)])
+def test_control_512_64_many_parts(gpu, T, topk, n_valid):
+    """Long lists over few tokens: each (token, head half) sequence spans up to seventeen CTAs,
+    so the head CTA merges up to sixteen parts, streamed through its idle code stages."""
+    wl = W.fp8_paged(T=T, requests=2, positions=8192, page_size=64, topk=topk, n_valid=n_valid, d_nope=512,
+                     d_rope=64, d_v=512, seed=70 + T + topk % 7, sm_scale=1 / 24, scatter_frac=0.5)
+    _check(wl, gpu)
+
+
 def test_control_512_64_paged_padded(gpu):
     wl = W.fp8_paged(T=5, requests=2, positions=4096, page_size=64, topk=2112, n_valid=2051, d_nope=512, d_rope=64,
                      d_v=512, seed=45, sm_scale=1 / 24, scatter_frac=0.4)
