@@ -1071,20 +1071,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 // that every CTA gets about the same work. Both read only the index lists; the bounds depend on nothing else, so a split
 // (and so the result) is the same on every call.
 
-// work of unit u (window [128 j, 128 j + 128) of token u / NT): a full tile if any entry is
-// >= 0 (a token's valid entries are packed into dense tiles, and a tile costs the same however
-// full), plus the token's fixed work on its first unit
-__device__ __forceinline__ int unit_work(const int32_t* idx, int64_t idx_stride, int topk, int NT, int64_t u, int lane) {
-  const int64_t t = u / NT;
-  const int j = (int)(u - t * NT);
-  const int32_t* row = idx + t * idx_stride;
-  bool any = false;
+// Work of units u0 .. u0 + 7 (unit u: window [128 j, 128 j + 128) of token u / NT): a full tile
+// if any entry is >= 0 (a token's valid entries are packed into dense tiles, and a tile costs the
+// same however full), plus the token's fixed work on its first unit; 0 past u1. The warp reads
+// each window's 128 entries (four per lane), all eight windows' loads in flight at once.
+constexpr int kUnitBatch = 8;
+__device__ __forceinline__ void unit_work8(const int32_t* idx, int64_t idx_stride, int topk, int NT, int64_t u0,
+                                           int64_t u1, int lane, int (&w)[kUnitBatch]) {
+  int v[kUnitBatch][4];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int e = kBN * j + 32 * k + lane;
-    any |= e < topk && row[e] >= 0;
+  for (int q = 0; q < kUnitBatch; ++q) {
+    const int64_t u = u0 + q;
+    const int64_t t = u / NT;
+    const int j = (int)(u - t * NT);
+    const int32_t* row = idx + t * idx_stride;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int e = kBN * j + 32 * k + lane;
+      v[q][k] = (u < u1 && e < topk) ? __ldg(row + e) : -1;
+    }
   }
-  return (__any_sync(0xffffffffu, any) ? kBN : 0) + (j == 0 ? kSegmentWeight : 0);
+#pragma unroll
+  for (int q = 0; q < kUnitBatch; ++q) {
+    const int64_t u = u0 + q;
+    const int64_t t = u / NT;
+    const int j = (int)(u - t * NT);
+    const bool any = (v[q][0] & v[q][1] & v[q][2] & v[q][3]) >= 0;  // not every sign bit set: some entry >= 0
+    const bool hit = __any_sync(0xffffffffu, any);
+    w[q] = u < u1 ? (hit ? kBN : 0) + (j == 0 ? kSegmentWeight : 0) : 0;
+  }
 }
 
 // warp s: work of slice s = units [s U / S, (s + 1) U / S)
@@ -1095,7 +1110,12 @@ __global__ void __launch_bounds__(1024) split_count_kernel(const int32_t* __rest
   if (s >= S) return;
   const int64_t u0 = (int64_t)s * U / S, u1 = (int64_t)(s + 1) * U / S;
   int64_t c = 0;
-  for (int64_t u = u0; u < u1; ++u) c += unit_work(idx, idx_stride, topk, NT, u, lane);
+  for (int64_t u = u0; u < u1; u += kUnitBatch) {
+    int w[kUnitBatch];
+    unit_work8(idx, idx_stride, topk, NT, u, u1, lane, w);
+#pragma unroll
+    for (int q = 0; q < kUnitBatch; ++q) c += w[q];
+  }
   if (lane == 0) tot[s] = c;
 }
 
@@ -1160,17 +1180,16 @@ __global__ void __launch_bounds__(256) split_bounds_kernel(const int32_t* __rest
   }
   const int64_t u0 = s * U / S, u1 = (s + 1) * U / S;
   int64_t bound = u1;
-  for (int64_t ub = u0; ub < u1; ub += 32) {  // 32 units a round, one per lane
+  for (int64_t ub = u0; ub < u1; ub += 32) {  // 32 units a round; lane i then holds unit ub + i's work
     const int64_t u = ub + lane;
     int c = 0;
-    if (u < u1) {
-      const int64_t t = u / NT;
-      const int j = (int)(u - t * NT);
-      const int32_t* row = idx + t * idx_stride;
-      const int e1 = min(topk, kBN * (j + 1));
-      bool any = false;
-      for (int e = kBN * j; e < e1 && !any; ++e) any = row[e] >= 0;
-      c = (any ? kBN : 0) + (j == 0 ? kSegmentWeight : 0);
+#pragma unroll 1
+    for (int b8 = 0; b8 < 32; b8 += kUnitBatch) {
+      int w[kUnitBatch];
+      unit_work8(idx, idx_stride, topk, NT, ub + b8, u1, lane, w);
+#pragma unroll
+      for (int q = 0; q < kUnitBatch; ++q)
+        if (lane == b8 + q) c = w[q];
     }
     int incl = c;
 #pragma unroll
