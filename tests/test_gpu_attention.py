@@ -131,6 +131,38 @@ def test_control_512_64_paged_padded(gpu):
     _check(wl, gpu)
 
 
+def test_control_512_64_edge_cases(gpu):
+    """The 512+64 FP8 control with: token 0 all entries masked, token 1 one valid entry, token 2
+    every entry the same slot, token 3 a list shorter than a tile, token 4 entries scattered
+    among -1 (and -7), token 5 an index past the cache (masked and flagged)."""
+    wl = W.fp8_direct(T=6, slots=3000, topk=2112, n_valid=2000, seed=47, sm_scale=1 / 24)
+    idx = wl.indices
+    idx[0, :] = -1
+    idx[1, :] = -1
+    idx[1, 1500] = 77
+    idx[2, :] = 555
+    idx[3, 90:] = -1
+    idx[4, ::3] = -7
+    idx[5, 2001] = 3000
+    cache = oracle_cache(wl)
+    err = torch.zeros(1, dtype=torch.int32, device=gpu)
+    out, lse_t = _gpu_attn(wl, cache, gpu, lse=True, err=err)
+    assert err.item() & dsa.DEVERR_INDEX_OUT_OF_RANGE
+    ref, ref_lse, bad = run_oracle(wl, cache)
+    assert bad == 1
+    check_close(f32_of(out), ref, "control edge cases (exact dequantisation)", max_abs=MAX_ABS_ORDER_ONE)
+    _check_lse(f32_of(lse_t), ref_lse, 2e-4)
+
+
+@pytest.mark.parametrize("sm_scale", [0.0, 0.5, -1 / 24])
+def test_control_512_64_scales(gpu, sm_scale):
+    """The control at scale 0 (the mean of the rows), at 0.5 (scores of order 10-40 on rows of
+    width 576: the lazy maxima of the row sums and of the four output quarters grow and rescale)
+    and at a negative scale."""
+    wl = W.fp8_direct(T=4, slots=4000, topk=2048, n_valid=2048, seed=48, sm_scale=sm_scale)
+    _check(wl, gpu, max_abs=MAX_ABS_ORDER_ONE if sm_scale > 0.1 else MAX_ABS)
+
+
 # -------------------------------------------------------------------------------- edge cases --
 def test_masked_single_duplicate_and_small_topk(gpu):
     """Token 0: all entries masked; token 1: one valid entry; token 2: every entry the same slot;
