@@ -97,7 +97,7 @@ def kernels_per_call(wl, sm_count):
         return 1
     nt = (wl.indices.shape[1] + 127) // 128
     u = wl.T * nt
-    g = min(sm_count, (u + 1) // 2)
+    g = min(sm_count, (u + 3) // 4)
     while g > 1 and (nt + u // g - 1) // (u // g) + 1 > 17:
         g -= 1
     gap = (nt + 14) // 15

@@ -1215,10 +1215,11 @@ dsa_status_t plan_unit_split(const dsa_attn_args_t* a, const DeviceInfo& dev, co
   UnitSplit r;
   r.NT = (a->topk + kBN - 1) / kBN;
   r.U = a->T * (int64_t)r.NT;
-  // one persistent CTA per SM, with at least 2 units per CTA (a small batch spreads over many
-  // CTAs: the parts of a split token are merged from bulk copies in shared memory), and few
-  // enough CTAs that a token spans at most kMaxParts + 1 of them
-  int64_t G = (r.U + 1) / 2;
+  // one persistent CTA per SM, with at least 4 units per CTA (a small batch spreads over
+  // several CTAs per token, whose parts the head CTA merges from bulk copies in shared memory:
+  // four units each measured faster than two for 8 and 17 tokens, fewer parts to merge against
+  // two more tiles), and few enough CTAs that a token spans at most kMaxParts + 1 of them
+  int64_t G = (r.U + 3) / 4;
   if (G > dev.sm_count) G = dev.sm_count;
   while (G > 1) {
     const int64_t upc = r.U / G;  // fewest units any CTA holds

@@ -249,13 +249,13 @@ def test_many_tokens_stream_split(gpu):
 
 
 @pytest.mark.parametrize("kind", [0, 1])
-@pytest.mark.parametrize("T", [2, 37, 74, 150])
-def test_split_token_merge_part_counts(gpu, kind, T):
-    """Batches whose tokens split into about eight, four, two and one extra part(s): the head
-    CTA's merge streams every part through its two shared-memory slot pairs (more than two
-    parts reuse them) and adds them in a fixed order."""
-    wl = W.fp8_paged(T=T, requests=2, positions=4096, page_size=64, topk=2048, n_valid=2000, seed=60 + T,
-                     sm_scale=1 / 16, scatter_frac=0.3)
+@pytest.mark.parametrize("T,topk", [(1, 8192), (2, 4096), (37, 2048), (74, 2048), (150, 2048)])
+def test_split_token_merge_part_counts(gpu, kind, T, topk):
+    """Batches whose tokens span up to sixteen, eight, four, three and two CTAs: the head CTA's
+    merge streams every part through its two shared-memory slot pairs (more than two parts
+    reuse them) and adds them in a fixed order."""
+    wl = W.fp8_paged(T=T, requests=2, positions=2 * topk, page_size=64, topk=topk, n_valid=topk - 48,
+                     seed=60 + T, sm_scale=1 / 16, scatter_frac=0.3)
     if kind == 0:
         wl.kind = 0
     _check(wl, gpu)
