@@ -1,7 +1,8 @@
 // dsa_attn.cu - DSA sparse MLA attention forward for sm_103a (tcgen05 + TMEM + TMA): the
 // entry points (argument checks, dispatch, workspace, fixed-scratch variant), the host pieces
-// shared with dsa_attn_k128.cu, and the kernel of the 512+64 control geometry. The 256+0
-// geometry runs in dsa_attn_k128.cu.
+// shared with the other attention files, and the kernel of the 512+64 control geometry over a
+// bf16 cache. The 256+0 geometry runs in dsa_attn_k128.cu (bf16) and dsa_attn_f8.cu (FP8), the
+// 512+64 geometry over the packed FP8 cache in dsa_attn_ctl.cu.
 //
 // What is computed (sglang PR #38547 "Enable zero-RoPE TileLang DSA on gfx950", Summary and
 // Direct GLM geometry coverage list): for every query token t and head h, gather the latent
@@ -9,7 +10,7 @@
 // softmax over j and return sum_j p_j * k_j[0:d_v] in bf16. The cache holds bf16 rows or the
 // packed scaled-FP8 rows of the Contract table (codes * per-128-tile fp32 scale).
 //
-// 512+64 kernel design:
+// 512+64 bf16 kernel design:
 //  * Heads are the MMA M dimension (M = 64), gathered keys are N: S = Q K^T (K-dim = d) and
 //    O += P V (K-dim = keys, V = the first d_v columns of the same gathered rows) are dense
 //    tcgen05 kind::f16 contractions with fp32 accumulators in tensor memory. The M = 64
@@ -20,10 +21,10 @@
 //    is finished by the CTA holding its first tiles, which merges the other CTAs' partial
 //    (o, max, sum) from the workspace in a fixed order (deterministic, no atomics on data).
 //  * Warp roles: warp 0 producer (index read, -1 compaction, page translation, L2 prefetch of
-//    index / block-table / FP8 rows, Q loads by TMA), warp 1 MMA issuer, warps 4-7 softmax +
-//    epilogue (one per TMEM sub-partition, 16 heads each), warps 8-15 row loaders: cp.async
-//    16-byte copies of bf16 rows, or loads of packed FP8 rows widened to bf16(code * scale),
-//    into the 128-byte-swizzled K-major tile.
+//    index / block-table rows, Q loads by TMA), warp 1 MMA issuer, warps 2-3 idle (they only
+//    follow the meta ring), warps 4-7 softmax + epilogue (one per TMEM sub-partition, 16 heads
+//    each), warps 8-15 row loaders: cp.async 16-byte copies of bf16 rows into the
+//    128-byte-swizzled K-major tile.
 //  * Online softmax in the exp2 domain with a lazy rescale (O and the running sum are only
 //    rescaled when the running max grows by more than 2^8).
 #include <cuda.h>
@@ -53,9 +54,8 @@ struct AttnCfg {
   static constexpr int KCH = DK / 64;              // 128-byte chunks along d
   static constexpr int PCH = (BN + 63) / 64;       // 128-byte chunks of P along keys
   static constexpr int HALF = BN / 2;              // keys per softmax thread
-  static constexpr int RB = D_NOPE + 4 * (D_NOPE / 128) + 2 * D_ROPE;
-  static constexpr int ROWB = KIND == DSA_CACHE_BF16 ? 2 * DK : RB;  // cache row bytes
-  static constexpr int NDEQ = 8;                   // loader warps (cp.async rows / FP8 dequant)
+  static_assert(KIND == DSA_CACHE_BF16, "the packed FP8 cache has its own kernels");
+  static constexpr int NDEQ = 8;                   // loader warps (cp.async rows)
   static constexpr int WARPS = 8 + NDEQ;
   static constexpr int THREADS = 32 * WARPS;
   static constexpr int IDX_PER_LANE = (BN + 31) / 32;
@@ -158,13 +158,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     for (int s = 0; s < C::KSTAGES; ++s) {
-      // bf16 rows: one cp.async arrive per loader thread; FP8 rows: one arrive per loader warp
-      mbar_init(k_full(s), C::KIND == DSA_CACHE_BF16 ? 32 * C::NDEQ : C::NDEQ);
+      mbar_init(k_full(s), 32 * C::NDEQ);  // one cp.async arrive per loader thread
       mbar_init(k_empty(s), 1);
     }
     for (int s = 0; s < C::MSTAGES; ++s) {
       mbar_init(m_full(s), 1);
-      mbar_init(m_empty(s), 1 + 2 + 4 + C::NDEQ);  // MMA thread, 2 prefetch, 4 softmax, loader warps
+      mbar_init(m_empty(s), 1 + 2 + 4 + C::NDEQ);  // MMA thread, warps 2-3, 4 softmax, loader warps
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(s_full(b), 1);
@@ -203,7 +202,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     // emits a meta entry with the compacted slot list. The index loads run two tiles ahead and
     // the block-table loads one tile ahead, so a tile (or a run of empty tiles) costs no
     // round trip of its own; both index rows and block-table rows are pulled into L2 at the
-    // segment start, and FP8 rows into L2 as soon as their slot is known.
+    // segment start.
     uint32_t mc = 0, qc = 0;
     const int64_t u0 = unit_begin(b, p.U, p.G), u1 = unit_begin(b + 1, p.U, p.G);
     auto emit_begin = [&](int& st) -> MetaHdr* {
@@ -413,8 +412,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       auto issue_s = [&](uint32_t gg) {
         const int ks = gg % C::KSTAGES;
         // bf16 rows arrive by cp.async, i.e. through the generic proxy: order them before the
-        // tensor core reads (the FP8 loaders fence on their side before arriving)
-        if constexpr (C::KIND == DSA_CACHE_BF16) fence_proxy_async_smem();
+        // tensor core reads
+        fence_proxy_async_smem();
         tc_fence_after();
         const uint64_t dK = sw128_desc(sbase + C::KT_OFF + ks * C::KT_BYTES, 16, 1024);
         // four k-steps at a time, so that a PV whose P became ready is not queued behind the
@@ -481,27 +480,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
     __syncwarp();
   } else if (warp == 2 || warp == 3) {
-    // ========================================================= L2 prefetch (2 warps) ====
-    // Packed FP8 rows are pulled into L2 as soon as their tile's slot list is published, a
-    // few tiles before the loader warps read them. One LSU prefetch per 128-byte line.
+    // ========================================================= idle (2 warps) ====
+    // These warps only follow the meta ring (its release counts them), so that they leave the
+    // loop with the others.
     uint32_t mc = 0;
-    const int pl = (warp - 2) * 32 + lane;  // 0..63
     while (!*abort_flag) {
       const int st = mc % C::MSTAGES;
       if (!wait(m_full(st), (mc / C::MSTAGES) & 1)) break;
       const MetaHdr* mh = reinterpret_cast<const MetaHdr*>(smem + C::META_OFF + st * C::META_BYTES);
       const int type = mh->type;
-      if constexpr (C::KIND == DSA_CACHE_FP8_SCALED) {
-        if (type == kTile) {
-          const int n_valid = mh->n_valid;
-          const int* slots = reinterpret_cast<const int*>(reinterpret_cast<const uint8_t*>(mh) + 32);
-          for (int r = pl; r < n_valid; r += 64) {
-            const uintptr_t r0 = reinterpret_cast<uintptr_t>(p.cache + (int64_t)slots[r] * C::RB);
-            for (uintptr_t a = r0 & ~uintptr_t(127); a < r0 + C::RB; a += 128)
-              asm volatile("prefetch.global.L2 [%0];" ::"l"(a > r0 ? a : r0));
-          }
-        }
-      }
       __syncwarp();
       if (lane == 0) mbar_arrive(m_empty(st));
       ++mc;
@@ -749,168 +736,51 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     // ====================================================== row loaders (8 warps) ====
     // Warp dw fills rows dw, dw + 8, ... of each K tile in the 128-byte-swizzled K-major layout
     // (row r, 16-byte granule g of 64-element chunk c at c*BN*128 + r*128 + ((g ^ (r&7)) << 4)).
-    // bf16 rows: cp.async 16-byte copies (rows past n_valid zero-filled), completion counted
-    // on the stage barrier per thread. Packed FP8 rows: codes and tile scales are loaded
-    // (already pulled into L2 by the producer), widened to bf16(code * scale) and stored.
+    // cp.async 16-byte copies (rows past n_valid zero-filled), completion counted on the stage
+    // barrier per thread.
     const int dw = warp - 8;
     constexpr int RPW = C::BN / C::NDEQ;  // rows per warp per tile
     uint32_t mc = 0, g = 0;
-    if constexpr (C::KIND == DSA_CACHE_BF16) {
-      while (!*abort_flag) {
-        const int st = mc % C::MSTAGES;
-        if (!wait(m_full(st), (mc / C::MSTAGES) & 1)) break;
-        const MetaHdr* mh = reinterpret_cast<const MetaHdr*>(smem + C::META_OFF + st * C::META_BYTES);
-        const int type = mh->type;
-        if (type != kTile) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(m_empty(st));
-          ++mc;
-          if (type == kDone) break;
-          continue;
-        }
-        const int n_valid = mh->n_valid;
-        const int* slots = reinterpret_cast<const int*>(reinterpret_cast<const uint8_t*>(mh) + 32);
-        const int ks = g % C::KSTAGES;
-        uint8_t* kt = smem + C::KT_OFF + ks * C::KT_BYTES;
-        if (g >= (uint32_t)C::KSTAGES && !wait(k_empty(ks), ((g / C::KSTAGES) & 1) ^ 1)) break;
-        constexpr int GR = C::DK / 8;  // 16-byte granules per row
-#pragma unroll 2
-        for (int k = 0; k < RPW; ++k) {
-          const int r = dw + C::NDEQ * k;
-          const bool v = r < n_valid;
-          const uint8_t* row = p.cache + (v ? (int64_t)slots[r] : 0) * (2 * C::DK);
-#pragma unroll
-          for (int q0 = 0; q0 < GR; q0 += 32) {
-            const int q = q0 + lane;
-            if (q < GR) {
-              const int ch = q >> 3, gr = q & 7;
-              const uint32_t dst = smem_u32(kt + ch * (C::BN * 128) + r * 128 + ((gr ^ (r & 7)) << 4));
-              asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(row + 16 * q),
-                           "r"(v ? 16 : 0)
-                           : "memory");
-            }
-          }
-        }
+    while (!*abort_flag) {
+      const int st = mc % C::MSTAGES;
+      if (!wait(m_full(st), (mc / C::MSTAGES) & 1)) break;
+      const MetaHdr* mh = reinterpret_cast<const MetaHdr*>(smem + C::META_OFF + st * C::META_BYTES);
+      const int type = mh->type;
+      if (type != kTile) {
         __syncwarp();
         if (lane == 0) mbar_arrive(m_empty(st));
         ++mc;
-        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(k_full(ks)) : "memory");
-        ++g;
+        if (type == kDone) break;
+        continue;
       }
-    } else {
-      // Packed FP8 rows, two tiles in flight per warp (256+0): the loads of the next tile are
-      // issued before the current tile is converted (two register buffers, used alternately).
-      constexpr int PARTS = C::D_NOPE / 256;
-      struct Rows {
-        uint2 codes[RPW][PARTS];
-        float scl[RPW][PARTS];
-        uint4 rope[RPW];
-        int n_valid;
-      };
-      // wait for the next tile's slot list (skipping segment ends), issue its row loads, and
-      // release the meta entry; false when the stream is done
-      // fetch() returns 1 when a tile was fetched, 0 at the end of the stream, and -1 (only
-      // when `block` is false) when the next entry is not published yet.
-      auto fetch = [&](Rows& R, bool block) -> int {
-        while (!*abort_flag) {
-          const int st = mc % C::MSTAGES;
-          if (!block && !mbar_test(m_full(st), (mc / C::MSTAGES) & 1)) return -1;
-          if (!wait(m_full(st), (mc / C::MSTAGES) & 1)) return 0;
-          const MetaHdr* mh = reinterpret_cast<const MetaHdr*>(smem + C::META_OFF + st * C::META_BYTES);
-          const int type = mh->type;
-          if (type == kTile) {
-            R.n_valid = mh->n_valid;
-            const int* slots = reinterpret_cast<const int*>(reinterpret_cast<const uint8_t*>(mh) + 32);
+      const int n_valid = mh->n_valid;
+      const int* slots = reinterpret_cast<const int*>(reinterpret_cast<const uint8_t*>(mh) + 32);
+      const int ks = g % C::KSTAGES;
+      uint8_t* kt = smem + C::KT_OFF + ks * C::KT_BYTES;
+      if (g >= (uint32_t)C::KSTAGES && !wait(k_empty(ks), ((g / C::KSTAGES) & 1) ^ 1)) break;
+      constexpr int GR = C::DK / 8;  // 16-byte granules per row
+#pragma unroll 2
+      for (int k = 0; k < RPW; ++k) {
+        const int r = dw + C::NDEQ * k;
+        const bool v = r < n_valid;
+        const uint8_t* row = p.cache + (v ? (int64_t)slots[r] : 0) * (2 * C::DK);
 #pragma unroll
-            for (int k = 0; k < RPW; ++k) {
-              const int r = dw + C::NDEQ * k;
-              if (r < R.n_valid) {
-                const uint8_t* row = p.cache + (int64_t)slots[r] * C::RB;
-#pragma unroll
-                for (int pt = 0; pt < PARTS; ++pt) {
-                  const int d0 = 256 * pt + 8 * lane;
-                  R.codes[k][pt] = __ldg(reinterpret_cast<const uint2*>(row + d0));
-                  R.scl[k][pt] = __ldg(reinterpret_cast<const float*>(row + C::D_NOPE + 4 * (d0 / 128)));
-                }
-                if constexpr (C::D_ROPE > 0) {
-                  if (lane < C::D_ROPE / 8)
-                    R.rope[k] = __ldg(reinterpret_cast<const uint4*>(row + C::D_NOPE + 4 * (C::D_NOPE / 128)) + lane);
-                }
-              }
-            }
+        for (int q0 = 0; q0 < GR; q0 += 32) {
+          const int q = q0 + lane;
+          if (q < GR) {
+            const int ch = q >> 3, gr = q & 7;
+            const uint32_t dst = smem_u32(kt + ch * (C::BN * 128) + r * 128 + ((gr ^ (r & 7)) << 4));
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(row + 16 * q),
+                         "r"(v ? 16 : 0)
+                         : "memory");
           }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(m_empty(st));
-          ++mc;
-          if (type == kTile) return 1;
-          if (type == kDone) return 0;
-        }
-        return 0;
-      };
-      // widen the rows of R into the next K stage and publish it
-      auto convert = [&](const Rows& R) -> bool {
-        const int ks = g % C::KSTAGES;
-        uint8_t* kt = smem + C::KT_OFF + ks * C::KT_BYTES;
-        if (g >= (uint32_t)C::KSTAGES && !wait(k_empty(ks), ((g / C::KSTAGES) & 1) ^ 1)) return false;
-#pragma unroll
-        for (int k = 0; k < RPW; ++k) {
-          const int r = dw + C::NDEQ * k;
-          const bool v = r < R.n_valid;
-#pragma unroll
-          for (int pt = 0; pt < PARTS; ++pt) {
-            const int d0 = 256 * pt + 8 * lane;
-            uint4 o = make_uint4(0, 0, 0, 0);
-            if (v) {
-              const float sc = R.scl[k][pt];
-              const uint32_t cw[2] = {R.codes[k][pt].x, R.codes[k][pt].y};
-              uint32_t w[4];
-#pragma unroll
-              for (int q = 0; q < 2; ++q) {
-                const float2 x0 = f16x2_to_f32x2(e4m3x2_to_f16x2((uint16_t)(cw[q] & 0xFFFFu)));
-                const float2 x1 = f16x2_to_f32x2(e4m3x2_to_f16x2((uint16_t)(cw[q] >> 16)));
-                w[2 * q] = f32x2_to_bf16x2(__fmul_rn(x0.x, sc), __fmul_rn(x0.y, sc));
-                w[2 * q + 1] = f32x2_to_bf16x2(__fmul_rn(x1.x, sc), __fmul_rn(x1.y, sc));
-              }
-              o = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-            const int ch = d0 >> 6, gr = (d0 & 63) >> 3;
-            *reinterpret_cast<uint4*>(kt + ch * (C::BN * 128) + r * 128 + ((gr ^ (r & 7)) << 4)) = o;
-          }
-          if constexpr (C::D_ROPE > 0) {
-            if (lane < C::D_ROPE / 8) {
-              const int ch = C::D_NOPE / 64 + (lane >> 3), gr = lane & 7;
-              *reinterpret_cast<uint4*>(kt + ch * (C::BN * 128) + r * 128 + ((gr ^ (r & 7)) << 4)) =
-                  v ? R.rope[k] : make_uint4(0, 0, 0, 0);
-            }
-          }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(k_full(ks));
-        ++g;
-        return true;
-      };
-      if constexpr (PARTS == 1) {
-        // The next tile is fetched ahead only when its entry is already published: waiting for
-        // it before converting the current tile could deadlock at a segment boundary (the next
-        // segment's first entry waits for its Q buffer, i.e. for this tile's S product).
-        Rows ra, rb;
-        int more = fetch(ra, true);
-        while (more == 1) {
-          int nb = fetch(rb, false);
-          if (!convert(ra)) break;
-          if (nb < 0) nb = fetch(rb, true);
-          if (nb == 0) break;
-          int na = fetch(ra, false);
-          if (!convert(rb)) break;
-          if (na < 0) na = fetch(ra, true);
-          more = na;
-        }
-      } else {  // 512+64 rows: one tile in flight (two would not fit in registers)
-        Rows ra;
-        while (fetch(ra, true) == 1 && convert(ra)) {
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(m_empty(st));
+      ++mc;
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(k_full(ks)) : "memory");
+      ++g;
     }
     // drain this thread's outstanding cp.async copies before the CTA can finish
     asm volatile("cp.async.wait_all;" ::: "memory");
