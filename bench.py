@@ -14,6 +14,7 @@ the same call with the step's inputs (q, indices) copied from pinned host memory
 copied back inside the timed region. ``cpu_baseline`` times the CPU oracle on a bounded sample.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5] [--impl reference]
+  python bench.py --op requant|proj|topk     (the other entry points, one JSON line each)
 """
 from __future__ import annotations
 
@@ -425,6 +426,77 @@ def run_requant(args, device):
     print(json.dumps(line))
 
 
+def run_topk(args, device):
+    """Timing of dsa_topk_select, the selection that produces the attention's index lists, on
+    two shapes: decode (256 rows of scores over 32768 positions, every position visible, K 2048)
+    and causal prefill (8192 rows over 8192 positions, row t seeing positions 0 .. t, K 2048).
+    Scores are seeded standard normals drawn on the device. One JSON line (decode) with the
+    prefill shape alongside; HBM-bound: the visible scores are read once and the lists written."""
+    import torch
+
+    import dsa_sparse_attention_mla_gb300 as dsa
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    hbm = _peaks()[0]
+
+    def shape(T, S, K, causal, seed):
+        gen = torch.Generator(device=device)
+        gen.manual_seed(seed)
+        scores = torch.randn((T, S), generator=gen, dtype=torch.float32, device=device)
+        lengths = (torch.arange(T, dtype=torch.int32, device=device) + 1).clamp_(max=S) if causal else None
+        out = torch.empty((T, K), dtype=torch.int32, device=device)
+
+        def step():
+            dsa.dsa_topk_select(scores, K, lengths=lengths, out=out)
+
+        for _ in range(args.warmup):
+            flush.fill_(1)
+            step()
+        torch.cuda.synchronize(device)
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        with ClockSampler(device) as clk:
+            for i in range(args.steps):
+                flush.fill_(i & 0xFF)
+                starts[i].record(stream)
+                step()
+                ends[i].record(stream)
+            torch.cuda.synchronize(device)
+        times = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+        ms = float(sum(times)) / args.steps
+        visible = sum(min(t + 1, S) for t in range(T)) if causal else T * S
+        nbytes = 4 * visible + 4 * T * K + (4 * T if causal else 0)
+        achieved = nbytes / (ms / 1000.0) / 1e9
+        name = f"topk_{'prefill' if causal else 'decode'}_T{T}_S{S}_k{K}"
+        res = {"metric": f"top-k selection rows/s ({name})", "value": T / (ms / 1000.0), "unit": "rows/s",
+               "ms_per_step": ms, "dtype": "f32 scores, int32 lists",
+               "config": {"workload": name, "rows": T, "positions": S, "k": K, "causal": causal,
+                          "l2": "512 MB buffer written between timed steps (outside the events)"},
+               "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                            "traffic": None, "algorithmic_bytes_per_launch": nbytes},
+               "gpu_launches": args.steps, "clocks": clk.summary(),
+               "step_ms": {"median": statistics.median(times), "min": min(times), "max": max(times)}}
+        return res, scores, lengths
+
+    dec, scores, _ = shape(256, 32768, 2048, False, 11)
+    pre, _, _ = shape(8192, 8192, 2048, True, 12)
+    # CPU baseline: the oracle's stable sort on a bounded sample of the decode rows
+    from oracle.selection import topk_select
+
+    host = scores[:16].cpu().numpy()
+    t0 = time.perf_counter()
+    topk_select(host, 2048)
+    cpu_rows_s = host.shape[0] / (time.perf_counter() - t0)
+    line = dict(dec)
+    line.update({"n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+                 "scaling": "weak", "vs_baseline": None, "data": "synthetic",
+                 "cpu_baseline": {"value": cpu_rows_s, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                                  "sample": "16 of the 256 decode rows", "cpu": cpu_model()},
+                 "prefill": pre})
+    print(json.dumps(line))
+
+
 def run_proj(args, device):
     """Timing of the FP8 block-scaled projection GEMM at prefill size (8192 tokens): q_b_proj
     (K 2048 -> N 16384 = 64 heads x 256) and o_proj (K 16384 -> N 6144); the pages name the layers
@@ -669,9 +741,9 @@ def main():
     ap.add_argument("--config", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--op", default="attn", choices=["attn", "requant", "proj"],
+    ap.add_argument("--op", default="attn", choices=["attn", "requant", "proj", "topk"],
                     help="requant: time dsa_gather_requant on the decode workload's rows instead; proj: the "
-                         "FP8 block-scaled projection GEMM")
+                         "FP8 block-scaled projection GEMM; topk: the top-k selection at decode and prefill shapes")
     ap.add_argument("--no-prefill", dest="prefill", action="store_false",
                     help="with the default decode workload, skip the second (T=8192 prefill) measurement")
     ap.add_argument("--no-extra", dest="extra", action="store_false",
@@ -728,9 +800,9 @@ def main():
     __graft_entry__.build() if rank == 0 else None
     if world > 1:
         torch.distributed.barrier()
-    if args.op in ("requant", "proj"):
+    if args.op in ("requant", "proj", "topk"):
         if rank == 0:
-            (run_requant if args.op == "requant" else run_proj)(args, device)
+            {"requant": run_requant, "proj": run_proj, "topk": run_topk}[args.op](args, device)
         if world > 1:
             torch.distributed.destroy_process_group()
         return

@@ -9,13 +9,16 @@
 // order with equal scores in ascending position order (-0.0 equals +0.0), then -1 up to K.
 //
 // Kernel: one CTA per row (1024 threads). Scores map to unsigned keys that order like the
-// floats. A four-pass radix select (8 bits per pass, most significant first, a shared-memory
-// histogram per pass) finds the K-th largest key u*; the keys above u* are collected in any order
-// (shared atomic counter) and the ties at u* in position order (a block-wide scan over the row in
-// position order), so the choice among equal scores is the lowest positions. The K selected
-// (key, position) pairs are then sorted by a bitonic network in shared memory on 64-bit words
-// (~key << 32 | position) and written out. Every decision is on integer keys: the result is the
-// same on every run.
+// floats; a row whose keys fit in shared memory (beside the sort buffer) is read from HBM once,
+// with many loads in flight, and every later pass reads the shared copy. A four-pass radix
+// select (8 bits per pass, most significant first; per pass each warp counts into its own
+// 256-entry histogram, since scores bunch in a few top digits and one shared histogram would
+// serialise the whole CTA on them; the 32 histograms are then summed and one warp scans the 256
+// counts) finds the K-th largest key u*; the keys above u* are collected in any order (one shared atomic per warp) and the ties at u* in position
+// order (a block-wide scan over the row in position order), so the choice among equal scores is
+// the lowest positions. The K selected (key, position) pairs are then sorted by a bitonic network
+// in shared memory on 64-bit words (~key << 32 | position) and written out. Every decision is on
+// integer keys: the result is the same on every run.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -27,7 +30,7 @@ namespace topk {
 
 constexpr int kThreads = 1024;
 constexpr int kMaxK = 16384;
-constexpr int kPerThread = 4;  // contiguous positions per thread in the ordered tie scan
+constexpr int kSmemMax = 225 * 1024;  // dynamic shared memory per CTA: sort buffer + cached keys
 
 // Unsigned key with the order of the float values (-0.0 maps as +0.0).
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -38,43 +41,109 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 // Ascending order of the composite = descending key, then ascending position.
 __device__ __forceinline__ uint64_t compose(uint32_t key, uint32_t pos) { return ((uint64_t)(~key) << 32) | pos; }
 
-// Exclusive scan of one value per thread over the block; returns the prefix and the total.
-__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int& total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int x = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += x;
-  }
-  if (lane == 31) warp_sums[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const int w = warp_sums[lane];  // kThreads / 32 == 32 warps
-    int wi = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int x = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += x;
+// Bitonic sort of buf[0 .. P) ascending, P a power of two, in shared memory: every thread takes
+// whole compare-exchange pairs (i, i + j) of each step. Ends synchronised.
+__device__ __forceinline__ void sort_smem(uint64_t* buf, int P) {
+  const int tid = threadIdx.x;
+  for (int k = 2; k <= P; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int q = tid; q < (P >> 1); q += kThreads) {
+        const int i = ((q & ~(j - 1)) << 1) | (q & (j - 1)), ixj = i | j;
+        const uint64_t a = buf[i], bv = buf[ixj];
+        const bool up = (i & k) == 0;
+        if ((a > bv) == up) {
+          buf[i] = bv;
+          buf[ixj] = a;
+        }
+      }
+      __syncthreads();
     }
-    warp_sums[lane] = wi - w;  // exclusive prefix of each warp
-    if (lane == 31) warp_sums[32] = wi;
+  }
+}
+
+// The same network with P = 1024 E (E = 2 or 4: K up to 4096): thread t holds elements E t .. E t + E - 1 in registers.
+// Steps whose partner is in the same thread (j < E) or the same warp (j < 32 E, a shuffle with
+// lane t ^ (j / E)) stay in registers; only the steps between warps go through shared memory.
+// The pair (i, i + j) of a step keeps the smaller word at i when (i & k) == 0, else the larger.
+// Ends with buf sorted and synchronised.
+template <int E>
+__device__ __forceinline__ void sort_regs(uint64_t* buf, int P) {
+  const int tid = threadIdx.x;
+  uint64_t v[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) v[e] = buf[E * tid + e];
+  for (int k = 2; k <= P; k <<= 1) {
+    int j = k >> 1;
+    if (j >= 32 * E) {
+      __syncthreads();  // every thread's reads of the previous layout are done
+#pragma unroll
+      for (int e = 0; e < E; ++e) buf[E * tid + e] = v[e];
+      __syncthreads();
+      for (; j >= 32 * E; j >>= 1) {
+        for (int q = tid; q < (P >> 1); q += kThreads) {
+          const int i = ((q & ~(j - 1)) << 1) | (q & (j - 1)), ixj = i | j;
+          const uint64_t a = buf[i], bv = buf[ixj];
+          const bool up = (i & k) == 0;
+          if ((a > bv) == up) {
+            buf[i] = bv;
+            buf[ixj] = a;
+          }
+        }
+        __syncthreads();
+      }
+#pragma unroll
+      for (int e = 0; e < E; ++e) v[e] = buf[E * tid + e];
+    }
+    // the direction bit (i & k) is the same for every slot of a thread from k = E on
+    const bool up_t = ((E * tid) & k) == 0;
+#pragma unroll
+    for (int lm = 16; lm >= 1; lm >>= 1) {  // j = lm * E: partner lane tid ^ lm, same slot
+      if (lm * E <= (k >> 1)) {
+        const bool take_max = ((tid & lm) == 0) != up_t;  // keep the larger word
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const uint64_t x = v[e];
+          const uint32_t plo = __shfl_xor_sync(0xffffffffu, (uint32_t)x, lm);
+          const uint32_t phi = __shfl_xor_sync(0xffffffffu, (uint32_t)(x >> 32), lm);
+          const uint64_t y = ((uint64_t)phi << 32) | plo;
+          v[e] = ((x < y) != take_max) ? x : y;
+        }
+      }
+    }
+#pragma unroll
+    for (int jj = E / 2; jj >= 1; jj >>= 1) {  // partner in the same thread
+      if (jj <= (k >> 1)) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          if ((e & jj) == 0) {
+            const uint64_t a = v[e], bv = v[e | jj];
+            const bool up = ((E * tid + e) & k) == 0;
+            if ((a > bv) == up) {
+              v[e] = bv;
+              v[e | jj] = a;
+            }
+          }
+        }
+      }
+    }
   }
   __syncthreads();
-  const int r = warp_sums[warp] + incl - v;
-  total = warp_sums[32];
-  __syncthreads();  // warp_sums is reused by the next call
-  return r;
+#pragma unroll
+  for (int e = 0; e < E; ++e) buf[E * tid + e] = v[e];
+  __syncthreads();
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     topk_kernel(const float* __restrict__ scores, int64_t S, int64_t stride, const int32_t* __restrict__ lengths, int K,
-                int P, int32_t* __restrict__ out, int64_t out_stride) {
-  extern __shared__ uint64_t buf[];  // P entries (P = next power of two >= K)
+                int P, int64_t kcap, int32_t* __restrict__ out, int64_t out_stride) {
+  extern __shared__ uint64_t buf[];  // P entries (P = next power of two >= K), 32 warp histograms, kcap keys
+  int* whist = reinterpret_cast<int*>(buf + P);  // [32 warps][256 digits]
+  uint32_t* keys = reinterpret_cast<uint32_t*>(whist + 32 * 256);
   __shared__ int hist[256];
   __shared__ int warp_sums[33];
+  __shared__ int s_cnt_t[32];
   __shared__ uint32_t s_prefix;
-  __shared__ int s_need, s_count;
+  __shared__ int s_need;
   const int tid = threadIdx.x;
   const int64_t t = blockIdx.x;
   const float* row = scores + t * stride;
@@ -84,30 +153,80 @@ __global__ void __launch_bounds__(kThreads, 1)
     n = l < 0 ? 0 : (l > S ? S : l);
   }
   int sel;  // positions selected
+  // the row's keys: from the shared copy when the row fits, else from global memory
+  const bool cached = n > K && n <= kcap;
+  if (cached) {
+    if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0) {  // 16-byte loads, four keys at a time
+      const int64_t n4 = n >> 2;
+      const float4* r4 = reinterpret_cast<const float4*>(row);
+      uint4* k4 = reinterpret_cast<uint4*>(keys);
+#pragma unroll 4
+      for (int64_t i = tid; i < n4; i += kThreads) {
+        const float4 f = __ldg(r4 + i);
+        k4[i] = make_uint4(order_key(f.x), order_key(f.y), order_key(f.z), order_key(f.w));
+      }
+      for (int64_t i = 4 * n4 + tid; i < n; i += kThreads) keys[i] = order_key(row[i]);
+    } else {
+#pragma unroll 8
+      for (int64_t i = tid; i < n; i += kThreads) keys[i] = order_key(row[i]);
+    }
+    __syncthreads();
+  }
+  auto key_at = [&](int64_t i) -> uint32_t { return cached ? keys[i] : order_key(row[i]); };
   if (n <= K) {
     sel = (int)n;
     for (int i = tid; i < sel; i += kThreads) buf[i] = compose(order_key(row[i]), (uint32_t)i);
   } else {
     // ---- radix select of the K-th largest key
+    const int lane = tid & 31, warp = tid >> 5;
+    const uint32_t lt_mask = (1u << lane) - 1u;
     uint32_t prefix = 0u, mask = 0u;
     int need = K;  // how many of the keys matching the prefix still have to be taken from the top
     for (int pass = 0; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
-      for (int i = tid; i < 256; i += kThreads) hist[i] = 0;
-      __syncthreads();
+      int* wh = whist + 256 * warp;
+      for (int i = lane; i < 256; i += 32) wh[i] = 0;
+      __syncwarp();
+#pragma unroll 4
       for (int64_t i = tid; i < n; i += kThreads) {
-        const uint32_t u = order_key(row[i]);
-        if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1);
+        const uint32_t u = key_at(i);
+        if ((u & mask) == prefix) atomicAdd(&wh[(u >> shift) & 255u], 1);
       }
       __syncthreads();
-      if (tid == 0) {
-        int above = 0, d = 255;
-        for (; d > 0; --d) {
-          if (above + hist[d] >= need) break;
-          above += hist[d];
+      if (tid < 256) {
+        int c = 0;
+#pragma unroll 8
+        for (int w = 0; w < 32; ++w) c += whist[256 * w + tid];
+        hist[tid] = c;
+      }
+      __syncthreads();
+      if (warp == 0) {
+        // lane l holds digits 255 - 8 l .. 248 - 8 l, top first; the chosen digit d is the first
+        // from the top at which the running count reaches `need`
+        int cnt[8], tot = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          cnt[j] = hist[255 - 8 * lane - j];
+          tot += cnt[j];
         }
-        s_prefix = prefix | ((uint32_t)d << shift);
-        s_need = need - above;
+        int incl = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int x = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += x;
+        }
+        int above = incl - tot;
+        if (above < need && need <= incl) {
+          int d = 255 - 8 * lane;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (above + cnt[j] >= need) break;
+            above += cnt[j];
+            --d;
+          }
+          s_prefix = prefix | ((uint32_t)d << shift);
+          s_need = need - above;
+        }
       }
       __syncthreads();
       prefix = s_prefix;
@@ -116,54 +235,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncthreads();
     }
     const uint32_t ustar = prefix;  // the K-th largest key; `need` ties at ustar complete the K
-    // ---- keys above u*: K - need of them, any order (the sort below orders them)
-    if (tid == 0) s_count = 0;
-    __syncthreads();
-    for (int64_t i = tid; i < n; i += kThreads) {
-      const uint32_t u = order_key(row[i]);
-      if (u > ustar) buf[atomicAdd(&s_count, 1)] = compose(u, (uint32_t)i);
-    }
-    __syncthreads();
-    const int base = K - need;
-    // ---- ties at u*: the `need` lowest positions, by a scan over the row in position order
-    int taken = 0;
-    for (int64_t c0 = 0; c0 < n && taken < need; c0 += (int64_t)kThreads * kPerThread) {
-      const int64_t i0 = c0 + (int64_t)tid * kPerThread;
-      int mine = 0;
-#pragma unroll
-      for (int k = 0; k < kPerThread; ++k)
-        if (i0 + k < n && order_key(row[i0 + k]) == ustar) ++mine;
-      int total;
-      int r = taken + block_exclusive_scan(mine, warp_sums, total);
-#pragma unroll
-      for (int k = 0; k < kPerThread; ++k) {
-        if (i0 + k < n && order_key(row[i0 + k]) == ustar) {
-          if (r < need) buf[base + r] = compose(ustar, (uint32_t)(i0 + k));
-          ++r;
-        }
+    // ---- the keys above u* (K - need of them) and the first `need` ties at u* in position
+    // order. Warp w takes the contiguous positions [w cs, (w + 1) cs): a first pass counts its
+    // keys above and at u*, a scan over the warps gives each warp its offsets, and a second pass
+    // writes them (ballot ranks: position order within the warp, and warps in position order).
+    {
+      const int64_t cs = ((n + 32 * 32 - 1) / (32 * 32)) * 32;  // a multiple of 32 positions per warp
+      const int64_t w0 = (int64_t)warp * cs, w1 = w0 + cs < n ? w0 + cs : n;
+      int na = 0, nt = 0;
+      for (int64_t c0 = w0; c0 < w1; c0 += 32) {
+        const int64_t i = c0 + lane;
+        const uint32_t u = i < w1 ? key_at(i) : 0u;
+        na += __popc(__ballot_sync(0xffffffffu, i < w1 && u > ustar));
+        nt += __popc(__ballot_sync(0xffffffffu, i < w1 && u == ustar));
       }
-      taken += total;
+      if (lane == 0) {
+        warp_sums[warp] = na;
+        s_cnt_t[warp] = nt;
+      }
+      __syncthreads();
+      if (warp == 0) {
+        const int a = warp_sums[lane], b = s_cnt_t[lane];
+        int ia = a, ib = b;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int xa = __shfl_up_sync(0xffffffffu, ia, o), xb = __shfl_up_sync(0xffffffffu, ib, o);
+          if (lane >= o) {
+            ia += xa;
+            ib += xb;
+          }
+        }
+        warp_sums[lane] = ia - a;  // exclusive offsets
+        s_cnt_t[lane] = ib - b;
+      }
+      __syncthreads();
+      int oa = warp_sums[warp], ot = s_cnt_t[warp];
+      const int base = K - need;  // the ties follow the keys above u*
+      for (int64_t c0 = w0; c0 < w1 && (oa < base || ot < need); c0 += 32) {
+        const int64_t i = c0 + lane;
+        const uint32_t u = i < w1 ? key_at(i) : 0u;
+        const bool ab = i < w1 && u > ustar, ti = i < w1 && u == ustar;
+        const uint32_t ba = __ballot_sync(0xffffffffu, ab), bt = __ballot_sync(0xffffffffu, ti);
+        if (ab) buf[oa + __popc(ba & lt_mask)] = compose(u, (uint32_t)i);
+        if (ti) {
+          const int r = ot + __popc(bt & lt_mask);
+          if (r < need) buf[base + r] = compose(ustar, (uint32_t)i);
+        }
+        oa += __popc(ba);
+        ot += __popc(bt);
+      }
     }
     sel = K;
   }
   // ---- bitonic sort of buf[0 .. P) (pad past `sel` with the largest word)
   for (int i = sel + tid; i < P; i += kThreads) buf[i] = ~0ull;
   __syncthreads();
-  for (int k = 2; k <= P; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = tid; i < P; i += kThreads) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const uint64_t a = buf[i], bv = buf[ixj];
-          const bool up = (i & k) == 0;
-          if ((a > bv) == up) {
-            buf[i] = bv;
-            buf[ixj] = a;
-          }
-        }
-      }
-      __syncthreads();
-    }
+  switch (P) {
+    case 2048: sort_regs<2>(buf, P); break;
+    case 4096: sort_regs<4>(buf, P); break;
+    default: sort_smem(buf, P); break;
   }
   int32_t* orow = out + t * out_stride;
   for (int i = tid; i < K; i += kThreads) orow[i] = i < sel ? (int32_t)(uint32_t)(buf[i] & 0xFFFFFFFFull) : -1;
@@ -192,17 +322,21 @@ extern "C" dsa_status_t dsa_topk_select(const float* scores, int64_t T, int64_t 
     if (dev.device < 0 || dev.device >= 64) return DSA_ERR_NO_DEVICE;
     std::lock_guard<std::mutex> lock(mu);
     if (!done[dev.device]) {
-      const cudaError_t e = cudaFuncSetAttribute(topk::topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)((size_t)topk::kMaxK * sizeof(uint64_t)));
+      const cudaError_t e =
+          cudaFuncSetAttribute(topk::topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, topk::kSmemMax);
       if (e != cudaSuccess) return cuda_fail(e);
       done[dev.device] = true;
     }
   }
   int P = 1;
   while (P < K) P <<= 1;
-  const size_t smem = (size_t)P * sizeof(uint64_t);
+  // keys cached per row: as many as fit beside the sort buffer, and no more than the row has
+  // (rows longer than that read global memory in every pass)
+  const int64_t room = ((int64_t)topk::kSmemMax - (int64_t)P * (int64_t)sizeof(uint64_t) - 32 * 256 * 4) / 4;
+  const int64_t kcap = S < room ? S : room;
+  const size_t smem = (size_t)P * sizeof(uint64_t) + 32 * 256 * 4 + (size_t)kcap * 4;
   topk::topk_kernel<<<(unsigned)T, topk::kThreads, smem, static_cast<cudaStream_t>(stream)>>>(
-      S > 0 ? scores : nullptr, S, score_stride_t, lengths, K, P, indices, idx_stride_t);
+      S > 0 ? scores : nullptr, S, score_stride_t, lengths, K, P, kcap, indices, idx_stride_t);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? DSA_OK : cuda_fail(e);
 }
