@@ -133,7 +133,10 @@ __device__ __forceinline__ void sort_regs(uint64_t* buf, int P) {
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// MINB: CTAs per SM the registers are budgeted for (2 when the shared memory lets two rows run
+// on an SM at once, which hides more of each row's synchronisation).
+template <int MINB>
+__global__ void __launch_bounds__(kThreads, MINB)
     topk_kernel(const float* __restrict__ scores, int64_t S, int64_t stride, const int32_t* __restrict__ lengths, int K,
                 int P, int64_t kcap, int32_t* __restrict__ out, int64_t out_stride) {
   extern __shared__ uint64_t buf[];  // P entries (P = next power of two >= K), 32 warp histograms, kcap keys
@@ -322,8 +325,9 @@ extern "C" dsa_status_t dsa_topk_select(const float* scores, int64_t T, int64_t 
     if (dev.device < 0 || dev.device >= 64) return DSA_ERR_NO_DEVICE;
     std::lock_guard<std::mutex> lock(mu);
     if (!done[dev.device]) {
-      const cudaError_t e =
-          cudaFuncSetAttribute(topk::topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, topk::kSmemMax);
+      cudaError_t e = cudaFuncSetAttribute(topk::topk_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, topk::kSmemMax);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(topk::topk_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, topk::kSmemMax);
       if (e != cudaSuccess) return cuda_fail(e);
       done[dev.device] = true;
     }
@@ -335,8 +339,14 @@ extern "C" dsa_status_t dsa_topk_select(const float* scores, int64_t T, int64_t 
   const int64_t room = ((int64_t)topk::kSmemMax - (int64_t)P * (int64_t)sizeof(uint64_t) - 32 * 256 * 4) / 4;
   const int64_t kcap = S < room ? S : room;
   const size_t smem = (size_t)P * sizeof(uint64_t) + 32 * 256 * 4 + (size_t)kcap * 4;
-  topk::topk_kernel<<<(unsigned)T, topk::kThreads, smem, static_cast<cudaStream_t>(stream)>>>(
-      S > 0 ? scores : nullptr, S, score_stride_t, lengths, K, P, kcap, indices, idx_stride_t);
+  const float* sp = S > 0 ? scores : nullptr;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (smem <= (size_t)(110 * 1024))  // two CTAs fit the SM's shared memory
+    topk::topk_kernel<2><<<(unsigned)T, topk::kThreads, smem, cs>>>(sp, S, score_stride_t, lengths, K, P, kcap, indices,
+                                                                     idx_stride_t);
+  else
+    topk::topk_kernel<1><<<(unsigned)T, topk::kThreads, smem, cs>>>(sp, S, score_stride_t, lengths, K, P, kcap, indices,
+                                                                     idx_stride_t);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? DSA_OK : cuda_fail(e);
 }
