@@ -660,7 +660,10 @@ def measure(args, wl, rank, world, device, config=None):
     return {
         "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(wl, work),
+        # the products' operand type: e4m3 codes (FP8 cache: both products on the tensor core's
+        # 8-bit kind, fp32 accumulation) or bf16
+        "vs_baseline": None, "dtype": "e4m3" if wl.kind == 1 else "bf16", "data": "synthetic",
+        "config": workload_config(wl, work),
         "roofline": roof,
         "cpu_baseline": {"value": cpu_v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample,
                          "cpu": cpu_model()},
