@@ -14,7 +14,7 @@ the same call with the step's inputs (q, indices) copied from pinned host memory
 copied back inside the timed region. ``cpu_baseline`` times the CPU oracle on a bounded sample.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5] [--impl reference]
-  python bench.py --op requant|proj|topk     (the other entry points, one JSON line each)
+  python bench.py --op requant|proj|topk|pack|dequant     (the other entry points, one JSON line each)
 """
 from __future__ import annotations
 
@@ -497,6 +497,108 @@ def run_topk(args, device):
     print(json.dumps(line))
 
 
+def _time_op(args, device, step):
+    """Mean time (ms) of `step` over args.steps calls between CUDA events on the current stream,
+    after args.warmup untimed calls, with the 512 MB L2 flush between calls (outside the events);
+    returns (ms, step times, clock summary)."""
+    import torch
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize(device)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(device) as clk:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(device)
+    times = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    return float(sum(times)) / args.steps, times, clk.summary()
+
+
+def run_cache_ops(args, device):
+    """Timing of the two cache kernels at the decode workload's sizes: --op pack packs 1,048,576
+    bf16 latent rows (256+0) into 264-byte rows scattered through a random slot map
+    (dsa_quant_k_cache); --op dequant gathers and widens the 524,288 rows the 256 decode tokens
+    name (dsa_gather_dequant, paged). One JSON line each, HBM-bound."""
+    import torch
+
+    import dsa_sparse_attention_mla_gb300 as dsa
+    import oracle
+    from dsa_sparse_attention_mla_gb300 import workloads as W
+
+    hbm = _peaks()[0]
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    if args.op == "pack":
+        n = 1 << 20
+        gen = torch.Generator(device=device)
+        gen.manual_seed(21)
+        kv = torch.randn((n, 256), generator=gen, device=device).to(torch.bfloat16)
+        loc = torch.randperm(n, generator=gen, device=device)
+        cache = torch.empty((n, 264), dtype=torch.uint8, device=device)
+
+        def step():
+            dsa.dsa_quant_k_cache(kv, out_loc=loc, cache=cache, error_word=err)
+
+        ms, times, clk = _time_op(args, device, step)
+        nbytes = n * (512 + 264 + 8)
+        host_kv = kv[:4096].view(torch.int16).cpu().numpy().view(np.uint16)
+        t0 = time.perf_counter()
+        oracle.quant_k_cache(host_kv, num_slots=4096, n_threads=1)
+        cpu_v = 4096 / (time.perf_counter() - t0)
+        name, metric, sample = "pack_256p0_rows1048576", "pack rows/s (256+0, 264-byte rows)", "4096 rows"
+    else:
+        wl = W.config(3, seed=0)
+        _, cache, _, bt, _ = build_device_inputs(wl, device)
+        valid = wl.indices >= 0
+        pos = torch.from_numpy(wl.indices[valid].astype(np.int32)).to(device)
+        req = torch.from_numpy(np.broadcast_to(wl.req_of_token[:, None], wl.indices.shape)[valid].astype(np.int32)).to(device)
+        n = int(pos.numel())
+        out = torch.empty((n, 256), dtype=torch.bfloat16, device=device)
+
+        def step():
+            dsa.dsa_gather_dequant(cache, wl.kind, wl.d_nope, wl.d_rope, pos, block_table=bt, page_size=wl.page_size,
+                                   req_of_index=req, out=out, error_word=err)
+
+        ms, times, clk = _time_op(args, device, step)
+        nbytes = n * (264 + 512 + 4 + 4)
+        from oracle.workload_inputs import cache_for_tokens
+
+        tok = np.arange(8)
+        host_cache = cache_for_tokens(wl, tok)
+        v8 = wl.indices[tok] >= 0
+        hp = wl.indices[tok][v8].astype(np.int32)
+        hr = np.broadcast_to(wl.req_of_token[tok][:, None], v8.shape)[v8].astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.gather_dequant(host_cache, oracle.CACHE_FP8_SCALED, wl.d_nope, wl.d_rope, hp, block_table=wl.block_table,
+                              page_size=wl.page_size, req_of_index=hr)
+        cpu_v = hp.size / (time.perf_counter() - t0)
+        name, metric = "dequant_" + wl.name, "gather-dequant rows/s (256+0 FP8 paged)"
+        sample = f"{hp.size} rows of 8 tokens"
+    if err.item() != 0:
+        raise RuntimeError(f"device error word {err.item()} during the benchmark")
+    achieved = nbytes / (ms / 1000.0) / 1e9
+    line = {
+        "metric": metric, "value": n / (ms / 1000.0), "unit": "rows/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": name, "rows": n, "l2": "512 MB buffer written between timed steps (outside the events)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": None, "algorithmic_bytes_per_launch": nbytes},
+        "cpu_baseline": {"value": cpu_v, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": sample,
+                         "cpu": cpu_model()},
+        "gpu_launches": args.steps, "clocks": clk,
+        "step_ms": {"median": statistics.median(times), "min": min(times), "max": max(times)},
+    }
+    print(json.dumps(line))
+
+
 def run_proj(args, device):
     """Timing of the FP8 block-scaled projection GEMM at prefill size (8192 tokens): q_b_proj
     (K 2048 -> N 16384 = 64 heads x 256) and o_proj (K 16384 -> N 6144); the pages name the layers
@@ -744,9 +846,10 @@ def main():
     ap.add_argument("--config", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--op", default="attn", choices=["attn", "requant", "proj", "topk"],
+    ap.add_argument("--op", default="attn", choices=["attn", "requant", "proj", "topk", "pack", "dequant"],
                     help="requant: time dsa_gather_requant on the decode workload's rows instead; proj: the "
-                         "FP8 block-scaled projection GEMM; topk: the top-k selection at decode and prefill shapes")
+                         "FP8 block-scaled projection GEMM; topk: the top-k selection at decode and prefill shapes; "
+                         "pack / dequant: the cache pack and the gather-dequant helper")
     ap.add_argument("--no-prefill", dest="prefill", action="store_false",
                     help="with the default decode workload, skip the second (T=8192 prefill) measurement")
     ap.add_argument("--no-extra", dest="extra", action="store_false",
@@ -803,9 +906,10 @@ def main():
     __graft_entry__.build() if rank == 0 else None
     if world > 1:
         torch.distributed.barrier()
-    if args.op in ("requant", "proj", "topk"):
+    if args.op in ("requant", "proj", "topk", "pack", "dequant"):
         if rank == 0:
-            {"requant": run_requant, "proj": run_proj, "topk": run_topk}[args.op](args, device)
+            {"requant": run_requant, "proj": run_proj, "topk": run_topk, "pack": run_cache_ops,
+             "dequant": run_cache_ops}[args.op](args, device)
         if world > 1:
             torch.distributed.destroy_process_group()
         return
