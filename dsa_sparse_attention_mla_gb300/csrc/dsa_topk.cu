@@ -10,15 +10,17 @@
 //
 // Kernel: one CTA per row (1024 threads). Scores map to unsigned keys that order like the
 // floats; a row whose keys fit in shared memory (beside the sort buffer) is read from HBM once,
-// with many loads in flight, and every later pass reads the shared copy. A four-pass radix
-// select (8 bits per pass, most significant first; per pass each warp counts into its own
-// 256-entry histogram, since scores bunch in a few top digits and one shared histogram would
-// serialise the whole CTA on them; the 32 histograms are then summed and one warp scans the 256
-// counts) finds the K-th largest key u*; the keys above u* are collected in any order (one shared atomic per warp) and the ties at u* in position
-// order (a block-wide scan over the row in position order), so the choice among equal scores is
-// the lowest positions. The K selected (key, position) pairs are then sorted by a bitonic network
-// in shared memory on 64-bit words (~key << 32 | position) and written out. Every decision is on
-// integer keys: the result is the same on every run.
+// with 16-byte loads, and every later pass reads the shared copy. A four-pass radix select (8
+// bits per pass, most significant first) finds the K-th largest key u*: per pass each warp counts
+// into its own 256-entry histogram (scores bunch in a few top digits, and one shared histogram
+// would serialise the whole CTA on them), the 32 histograms are summed and one warp picks the
+// digit. The keys above u* and the first ties at u* are collected in position order from
+// per-warp chunks (a count pass, a scan over the warps, a write pass), so the choice among equal
+// scores is the lowest positions. The K selected (key, position) pairs are then sorted by a
+// bitonic network on 64-bit words (~key << 32 | position), in registers with shuffles for the
+// steps inside a warp and shared memory for the steps between warps, and written out. Rows that
+// fit two to an SM run two per SM. Every decision is on integer keys: the result is the same on
+// every run.
 #include <cuda_runtime.h>
 
 #include <mutex>
