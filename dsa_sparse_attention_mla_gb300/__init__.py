@@ -352,8 +352,7 @@ def dsa_sparse_attn_static_ws(q, cache, kind: int, indices, sm_scale: float, *, 
     """dsa_sparse_attn without a workspace: the library's fixed device scratch is used, so the
     call allocates no device memory (``out`` aside, when the caller passes none). For callers
     that cannot allocate device memory when they call; the first call on a device does one-time
-    set-up and should come before any stream capture. Calls whose kernels may overlap on the GPU
-    share the one scratch array and race on it."""
+    set-up. Calls whose kernels may overlap on the GPU share the one scratch array and race on it."""
     d_v = d_nope if d_v is None else d_v
     cache, out = _prepare_attn(q, cache, kind, indices, d_v, block_table, req_of_token, out, lse, error_word)
     a = _attn_args(q, cache, kind, indices, sm_scale, d_nope, d_rope, d_v, block_table, page_size, req_of_token,

@@ -234,7 +234,7 @@ DSA_API dsa_status_t dsa_sparse_attn(const dsa_attn_args_t* args, void* stream);
  *
  * The first call on each device does one-time set-up: it looks up the array's device address
  * (cudaGetSymbolAddress) and sets the attention kernels' shared-memory limits on that device.
- * Make that first call, per device, before any stream capture. All calls share the one array,
+ * All calls share the one array,
  * which keeps what the last call left there: a call tags the flags it sets with a fresh value
  * and clears every flag it consumes, so nothing has to be cleared between calls. Two calls
  * whose kernels overlap on the GPU (different streams, no ordering between them) race on the
