@@ -33,6 +33,7 @@ namespace topk {
 constexpr int kThreads = 1024;
 constexpr int kMaxK = 16384;
 constexpr int kSmemMax = 225 * 1024;  // dynamic shared memory per CTA: sort buffer + cached keys
+constexpr int kCandCap = 2048;        // keys left after two radix passes that the one-SM rows keep aside
 
 // Unsigned key with the order of the float values (-0.0 maps as +0.0).
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -141,14 +142,15 @@ template <int MINB>
 __global__ void __launch_bounds__(kThreads, MINB)
     topk_kernel(const float* __restrict__ scores, int64_t S, int64_t stride, const int32_t* __restrict__ lengths, int K,
                 int P, int64_t kcap, int32_t* __restrict__ out, int64_t out_stride) {
-  extern __shared__ uint64_t buf[];  // P entries (P = next power of two >= K), 32 warp histograms, kcap keys
+  extern __shared__ uint64_t buf[];  // P entries (P = next power of two >= K), 32 warp histograms, candidates, kcap keys
   int* whist = reinterpret_cast<int*>(buf + P);  // [32 warps][256 digits]
-  uint32_t* keys = reinterpret_cast<uint32_t*>(whist + 32 * 256);
+  uint2* cand = reinterpret_cast<uint2*>(whist + 32 * 256);  // [kCandCap] (key, position)
+  uint32_t* keys = reinterpret_cast<uint32_t*>(cand + kCandCap);
   __shared__ int hist[256];
   __shared__ int warp_sums[33];
   __shared__ int s_cnt_t[32];
   __shared__ uint32_t s_prefix;
-  __shared__ int s_need;
+  __shared__ int s_need, s_cand;
   const int tid = threadIdx.x;
   const int64_t t = blockIdx.x;
   const float* row = scores + t * stride;
@@ -187,18 +189,35 @@ __global__ void __launch_bounds__(kThreads, MINB)
     const uint32_t lt_mask = (1u << lane) - 1u;
     uint32_t prefix = 0u, mask = 0u;
     int need = K;  // how many of the keys matching the prefix still have to be taken from the top
+    // One-SM rows (long rows): after two passes over the row, one more pass sets aside the keys
+    // that already rank above the 16-bit prefix of u* (into the list, any order) and the keys
+    // that match it (candidates, when at most kCandCap); passes 2 and 3 and the final collection
+    // then read only the candidates. na16 / nc16: this warp's keys above / at the prefix, read
+    // off its histograms (positions warp * 32 + lane + 1024 k).
+    int na16 = 0, nc16 = 0;
+    bool filtered = false;
+    int ncand = 0, abv16 = 0;  // candidates, and the keys above the 16-bit prefix (written first)
     for (int pass = 0; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
       int* wh = whist + 256 * warp;
-      for (int i = lane; i < 256; i += 32) wh[i] = 0;
-      __syncwarp();
+      if (!filtered) {
+        for (int i = lane; i < 256; i += 32) wh[i] = 0;
+        __syncwarp();
 #pragma unroll 4
-      for (int64_t i = tid; i < n; i += kThreads) {
-        const uint32_t u = key_at(i);
-        if ((u & mask) == prefix) atomicAdd(&wh[(u >> shift) & 255u], 1);
+        for (int64_t i = tid; i < n; i += kThreads) {
+          const uint32_t u = key_at(i);
+          if ((u & mask) == prefix) atomicAdd(&wh[(u >> shift) & 255u], 1);
+        }
+      } else {
+        for (int i = tid; i < 256; i += kThreads) hist[i] = 0;
+        __syncthreads();
+        for (int j = tid; j < ncand; j += kThreads) {
+          const uint32_t u = cand[j].x;
+          if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1);
+        }
       }
       __syncthreads();
-      if (tid < 256) {
+      if (!filtered && tid < 256) {
         int c = 0;
 #pragma unroll 8
         for (int w = 0; w < 32; ++w) c += whist[256 * w + tid];
@@ -231,27 +250,110 @@ __global__ void __launch_bounds__(kThreads, MINB)
           }
           s_prefix = prefix | ((uint32_t)d << shift);
           s_need = need - above;
+          s_cand = hist[d];  // keys matching the new prefix
         }
       }
       __syncthreads();
       prefix = s_prefix;
       need = s_need;
+      if constexpr (MINB == 1) {
+        if (pass <= 1) {
+          const uint32_t dsel = (prefix >> shift) & 255u;
+          int a = 0;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) a += (uint32_t)(8 * lane + j) > dsel ? wh[8 * lane + j] : 0;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+          na16 += a;
+          if (pass == 1) nc16 = wh[dsel];
+        }
+      }
       mask |= 255u << shift;
       __syncthreads();
+      if constexpr (MINB == 1) {
+        if (pass == 1 && s_cand <= kCandCap) {
+          // the pass that sets the keys aside: per-warp offsets by a scan of na16 / nc16
+          if (lane == 0) {
+            warp_sums[warp] = na16;
+            s_cnt_t[warp] = nc16;
+          }
+          __syncthreads();
+          if (warp == 0) {
+            const int a = warp_sums[lane], b2 = s_cnt_t[lane];
+            int ia = a, ib = b2;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const int xa = __shfl_up_sync(0xffffffffu, ia, o), xb = __shfl_up_sync(0xffffffffu, ib, o);
+              if (lane >= o) {
+                ia += xa;
+                ib += xb;
+              }
+            }
+            warp_sums[lane] = ia - a;
+            s_cnt_t[lane] = ib - b2;
+          }
+          __syncthreads();
+          int oa = warp_sums[warp], oc = s_cnt_t[warp];
+          for (int64_t c0 = 32 * warp; c0 < n; c0 += kThreads) {
+            const int64_t i = c0 + lane;
+            const uint32_t u = i < n ? key_at(i) : 0u;
+            const bool ab = i < n && (u & mask) > prefix, cd = i < n && (u & mask) == prefix;
+            const uint32_t ba = __ballot_sync(0xffffffffu, ab), bc = __ballot_sync(0xffffffffu, cd);
+            if (ab) buf[oa + __popc(ba & lt_mask)] = compose(u, (uint32_t)i);
+            if (cd) cand[oc + __popc(bc & lt_mask)] = make_uint2(u, (uint32_t)i);
+            oa += __popc(ba);
+            oc += __popc(bc);
+          }
+          ncand = s_cand;
+          abv16 = K - need;
+          filtered = true;
+          __syncthreads();
+        }
+      }
     }
     const uint32_t ustar = prefix;  // the K-th largest key; `need` ties at ustar complete the K
+    const int base = K - need;      // the ties follow the keys above u*
+    bool ties_left = true;          // the position-ordered tie pass below still has to run
+    if (filtered) {
+      // the candidates above u* after the keys set aside, and the ties too when every one of
+      // them is taken (warp-aggregated slots; the sort orders them)
+      const bool all_ties = s_cand == need;
+      if (tid == 0) {
+        s_cnt_t[0] = 0;
+        s_cnt_t[1] = 0;
+      }
+      __syncthreads();
+      for (int j0 = 0; j0 < ncand; j0 += kThreads) {
+        const int j = j0 + tid;
+        const uint2 c = j < ncand ? cand[j] : make_uint2(0u, 0u);
+        const bool ab = j < ncand && c.x > ustar, ti = all_ties && j < ncand && c.x == ustar;
+        const uint32_t ba = __ballot_sync(0xffffffffu, ab), bt = __ballot_sync(0xffffffffu, ti);
+        int wa = 0, wt = 0;
+        if (lane == 0) {
+          if (ba) wa = atomicAdd(&s_cnt_t[0], __popc(ba));
+          if (bt) wt = atomicAdd(&s_cnt_t[1], __popc(bt));
+        }
+        wa = __shfl_sync(0xffffffffu, wa, 0);
+        wt = __shfl_sync(0xffffffffu, wt, 0);
+        if (ab) buf[abv16 + wa + __popc(ba & lt_mask)] = compose(c.x, c.y);
+        if (ti) buf[base + wt + __popc(bt & lt_mask)] = compose(c.x, c.y);
+      }
+      ties_left = !all_ties;
+      __syncthreads();
+    }
     // ---- the keys above u* (K - need of them) and the first `need` ties at u* in position
     // order. Warp w takes the contiguous positions [w cs, (w + 1) cs): a first pass counts its
     // keys above and at u*, a scan over the warps gives each warp its offsets, and a second pass
     // writes them (ballot ranks: position order within the warp, and warps in position order).
-    {
+    if (ties_left) {
+      const bool take_above = !filtered;  // (set aside and collected above otherwise)
       const int64_t cs = ((n + 32 * 32 - 1) / (32 * 32)) * 32;  // a multiple of 32 positions per warp
       const int64_t w0 = (int64_t)warp * cs, w1 = w0 + cs < n ? w0 + cs : n;
       int na = 0, nt = 0;
       for (int64_t c0 = w0; c0 < w1; c0 += 32) {
         const int64_t i = c0 + lane;
         const uint32_t u = i < w1 ? key_at(i) : 0u;
-        na += __popc(__ballot_sync(0xffffffffu, i < w1 && u > ustar));
+        na += __popc(__ballot_sync(0xffffffffu, take_above && i < w1 && u > ustar));
         nt += __popc(__ballot_sync(0xffffffffu, i < w1 && u == ustar));
       }
       if (lane == 0) {
@@ -275,11 +377,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
       }
       __syncthreads();
       int oa = warp_sums[warp], ot = s_cnt_t[warp];
-      const int base = K - need;  // the ties follow the keys above u*
-      for (int64_t c0 = w0; c0 < w1 && (oa < base || ot < need); c0 += 32) {
+      for (int64_t c0 = w0; c0 < w1 && ((take_above && oa < base) || ot < need); c0 += 32) {
         const int64_t i = c0 + lane;
         const uint32_t u = i < w1 ? key_at(i) : 0u;
-        const bool ab = i < w1 && u > ustar, ti = i < w1 && u == ustar;
+        const bool ab = take_above && i < w1 && u > ustar, ti = i < w1 && u == ustar;
         const uint32_t ba = __ballot_sync(0xffffffffu, ab), bt = __ballot_sync(0xffffffffu, ti);
         if (ab) buf[oa + __popc(ba & lt_mask)] = compose(u, (uint32_t)i);
         if (ti) {
@@ -338,9 +439,10 @@ extern "C" dsa_status_t dsa_topk_select(const float* scores, int64_t T, int64_t 
   while (P < K) P <<= 1;
   // keys cached per row: as many as fit beside the sort buffer, and no more than the row has
   // (rows longer than that read global memory in every pass)
-  const int64_t room = ((int64_t)topk::kSmemMax - (int64_t)P * (int64_t)sizeof(uint64_t) - 32 * 256 * 4) / 4;
+  const int64_t room =
+      ((int64_t)topk::kSmemMax - (int64_t)P * (int64_t)sizeof(uint64_t) - 32 * 256 * 4 - topk::kCandCap * 8) / 4;
   const int64_t kcap = S < room ? S : room;
-  const size_t smem = (size_t)P * sizeof(uint64_t) + 32 * 256 * 4 + (size_t)kcap * 4;
+  const size_t smem = (size_t)P * sizeof(uint64_t) + 32 * 256 * 4 + topk::kCandCap * 8 + (size_t)kcap * 4;
   const float* sp = S > 0 ? scores : nullptr;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (smem <= (size_t)(110 * 1024))  // two CTAs fit the SM's shared memory

@@ -45,6 +45,23 @@ def test_heavy_ties_take_the_lowest_positions(gpu):
     assert np.array_equal(got, topk_select(scores, K))
 
 
+@pytest.mark.parametrize("distinct", [8, 64, 1000])
+def test_heavy_ties_long_rows(gpu, distinct):
+    """Rows of 32768 positions (the one-row-per-SM kernel, which sets the keys matching the top
+    16 bits of the K-th largest aside after two radix passes): with 8 distinct values those keys
+    overflow the set-aside list and the row takes the full passes; with 64 and 1000 they fit, and
+    the ties at the K-th largest value outnumber the places left, so the lowest positions must
+    be taken in order."""
+    rng = np.random.default_rng(100 + distinct)
+    T, S = 12, 32768
+    for K in (2048, 2112):
+        scores = (rng.integers(0, distinct, size=(T, S)) * 0.125).astype(np.float32)
+        lengths = rng.integers(K + 1, S + 1, size=T)
+        lengths[0] = S
+        got = _gpu(scores, K, lengths, gpu)
+        assert np.array_equal(got, topk_select(scores, K, lengths))
+
+
 def test_signed_zeros_infinities_and_short_rows(gpu):
     rng = np.random.default_rng(6)
     pool = np.array([-np.inf, -2.0, -0.0, 0.0, 3.0, np.inf], dtype=np.float32)
