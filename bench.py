@@ -69,7 +69,7 @@ def job_value(world: int, tokens_per_rank: int, steps: int, total_ms: float) -> 
 def _recorded_traffic(workload):
     """DRAM bytes per launch of the attention kernel for this workload, from the ncu capture
     recorded under profiles/, or None when there is none or the kernel sources have changed
-    since it was taken (the record carries a hash of the sources it was measured on)."""
+    since it was taken (the record carries a hash of the source files of the measured kernels)."""
     import hashlib
 
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
@@ -78,12 +78,16 @@ def _recorded_traffic(workload):
     with open(path) as f:
         rec = json.load(f)
     src = os.path.join(ROOT, "dsa_sparse_attention_mla_gb300", "csrc")
+    # the record names the source files of the kernels it measured (every file when it names none)
+    names = rec.get("sources") or [n for n in os.listdir(src) if n.endswith((".cu", ".cuh", ".h", ".cpp"))]
     h = hashlib.sha256()
-    for name in sorted(os.listdir(src)):
-        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
-            h.update(name.encode())
-            with open(os.path.join(src, name), "rb") as f:
-                h.update(f.read())
+    for name in sorted(names):
+        path = os.path.join(src, name)
+        if not os.path.exists(path):
+            return None
+        h.update(name.encode())
+        with open(path, "rb") as f:
+            h.update(f.read())
     if h.hexdigest() != rec.get("csrc_sha256"):
         return None
     w = rec.get("workloads", {}).get(workload)
