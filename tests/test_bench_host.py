@@ -37,6 +37,31 @@ def test_recorded_traffic_tracks_kernel_sources(tmp_path, monkeypatch):
     assert bench._recorded_traffic("w") is None
 
 
+def test_recorded_traffic_follows_only_the_listed_sources(tmp_path, monkeypatch):
+    # a record that lists its kernels' files ignores the other files and voids on a listed one
+    root = tmp_path
+    src = root / "dsa_sparse_attention_mla_gb300" / "csrc"
+    src.mkdir(parents=True)
+    (src / "a.cu").write_text("measured v1")
+    (src / "b.cu").write_text("other v1")
+    (root / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    import hashlib
+
+    h = hashlib.sha256()
+    h.update(b"a.cu")
+    h.update(b"measured v1")
+    rec = {"csrc_sha256": h.hexdigest(), "sources": ["a.cu"], "workloads": {"w": {"traffic": 99}}}
+    (root / "profiles" / "dram_traffic.json").write_text(json.dumps(rec))
+    assert bench._recorded_traffic("w") == 99
+    (src / "b.cu").write_text("other v2")
+    assert bench._recorded_traffic("w") == 99
+    (src / "a.cu").write_text("measured v2")
+    assert bench._recorded_traffic("w") is None
+    (src / "a.cu").unlink()
+    assert bench._recorded_traffic("w") is None
+
+
 def test_kernels_per_call_follows_the_launch_rule():
     # decode T=256 x 17 windows on 152 SMs: 28 units per CTA, one launch; causal prefill
     # T=8192 x 16 windows: 862 units per CTA, split pre-pass + attention; 512+64: one launch
