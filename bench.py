@@ -103,6 +103,9 @@ def kernels_per_call(wl, sm_count):
     nt = (wl.indices.shape[1] + 127) // 128
     u = wl.T * nt
     g = min(sm_count, (u + 3) // 4)
+    k = max(1, nt // 4)
+    if wl.T * k <= sm_count:
+        g = wl.T * k
     while g > 1 and (nt + u // g - 1) // (u // g) + 1 > 17:
         g -= 1
     gap = (nt + 14) // 15

@@ -1221,6 +1221,12 @@ dsa_status_t plan_unit_split(const dsa_attn_args_t* a, const DeviceInfo& dev, co
   // two more tiles), and few enough CTAs that a token spans at most kMaxParts + 1 of them
   int64_t G = (r.U + 3) / 4;
   if (G > dev.sm_count) G = dev.sm_count;
+  {
+    // when every token can have the same whole number of CTAs, the ranges fall on token
+    // boundaries: no CTA holds the end of one token and the start of the next (two epilogues)
+    const int64_t k = r.NT / 4 > 0 ? r.NT / 4 : 1;
+    if (a->T * k <= dev.sm_count) G = a->T * k;
+  }
   while (G > 1) {
     const int64_t upc = r.U / G;  // fewest units any CTA holds
     if ((r.NT + upc - 1) / upc + 1 <= kMaxParts + 1) break;
